@@ -196,11 +196,19 @@ def kv_cache(w: Workload, num_pages: int):
     rng.permutation(1)  # keep the stream distinct from the page shuffle's draw
     shape = (num_pages, w.page_size, w.Hkv, w.Dh)
     out = {}
+    block = max(1, (1 << 24) // (w.page_size * w.Hkv * w.Dh))   # ~16M values per draw
     for name in ("k_cache", "v_cache"):
-        x = rng.standard_normal(shape, dtype=np.float32)
-        out[name] = f32_to_bf16_bits(x)
-        if w.qkv_fp32_source:
-            out[name + "_f32"] = x
+        bits = np.empty(shape, dtype=np.uint16)
+        f32 = np.empty(shape, dtype=np.float32) if w.qkv_fp32_source else None
+        for p0 in range(0, num_pages, block):
+            p1 = min(num_pages, p0 + block)
+            x = rng.standard_normal((p1 - p0,) + shape[1:], dtype=np.float32)
+            bits[p0:p1] = f32_to_bf16_bits(x)
+            if f32 is not None:
+                f32[p0:p1] = x
+        out[name] = bits
+        if f32 is not None:
+            out[name + "_f32"] = f32
     return out
 
 

@@ -1,0 +1,254 @@
+/*
+ * ddtree.h - C ABI of the DDTree tree-verify step on one GB300 (sm_103a).
+ *
+ * The step has four calls, taken in this order for one speculative-decoding
+ * step of a batch of B requests:
+ *
+ *   ddtree_build          per-depth top-k  -> best-first tree, mask, positions
+ *   tree_verify_attn      tree rows attend to their context (paged KV, read
+ *                         once per request and KV head) plus visible tree rows
+ *   ddtree_accept_greedy  longest root path matching the target argmax + bonus
+ *   ddtree_accept_sample  the same at temperature, by recursive rejection
+ *                         sampling over siblings + a bonus from the residual
+ *
+ * Sources (page titles; sections named at each call):
+ *   [Arch]   "The Architecture of Speculative Decoding: Dissecting DDTree's
+ *            Tree-Parallel Evaluation Strategy"
+ *   [Verify] "The Architecture of Speculative Verification: Implementing
+ *            Temperature-Aware Tree Sampling for DDTree"
+ *   [Pivot]  "The Pivot Point: Strategic Decision-Making in Speculative
+ *            Decoding Optimization"
+ *   [Branch] "The Tree That Couldn't Branch: Diagnosing a 2x Acceptance
+ *            Regression in DDTree Speculative Decoding"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every array pointer is DEVICE memory owned by the caller; the library
+ *   allocates nothing, keeps no pointer after the call returns, and writes
+ *   only the outputs (and the caller-provided workspace) it documents.
+ * - Arrays are dense, row-major (C order), with the shapes given; no strides.
+ * - bf16 arrays hold raw bfloat16 bit patterns (ddtree_bf16).
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream). Calls are asynchronous on it, never synchronise the host and
+ *   allocate nothing, so a sequence of calls with fixed sizes can be captured
+ *   in a CUDA graph.
+ * - Return value: DDT_OK, or a negative ddtree_status. Argument checks happen
+ *   on the host before any launch; on an argument error nothing is launched
+ *   and no output is written.
+ * - `dev_status` (nullable, one int32 in device memory): data errors found on
+ *   the device (a page id outside the pool, a token outside the vocabulary,
+ *   a malformed tree, a bad temperature) are OR-ed into it as DDT_DEV_* bits;
+ *   the library never clears it. The affected rows get defined, harmless
+ *   outputs (zeros or -1) and no out-of-bounds access is made. Nothing traps.
+ * - N = budget + 1 tree rows per request, W = (N + 31) / 32 mask words.
+ * - Sizes are plain int; every element count must fit in int64.
+ */
+#ifndef DDTREE_H
+#define DDTREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t ddtree_bf16;
+
+enum ddtree_status {
+    DDT_OK = 0,
+    DDT_EINVAL = -1,      /* null pointer or bad scalar argument              */
+    DDT_ESHAPE = -2,      /* sizes outside the supported range                */
+    DDT_ECUDA = -3,       /* a CUDA runtime call or launch failed             */
+    DDT_ETIMEOUT = -4,    /* reserved: a bounded device wait gave up          */
+    DDT_EWORKSPACE = -6   /* workspace pointer null or smaller than required  */
+};
+
+/* bits OR-ed into *dev_status by the device */
+enum ddtree_device_error {
+    DDT_DEV_BAD_PAGE = 1,         /* page_table entry < 0 or >= num_pages       */
+    DDT_DEV_BAD_CTX = 2,          /* ctx_len < 0 or > max_pages * page_size     */
+    DDT_DEV_BAD_TREE = 4,         /* tree arrays inconsistent (child index out  */
+                                  /* of range, walk longer than D, n_nodes > N) */
+    DDT_DEV_BAD_TEMPERATURE = 8,  /* temperature <= 0 or not finite             */
+    DDT_DEV_BAD_TOKEN = 16        /* token id outside [0, V)                    */
+};
+
+/* Limits checked on the host (DDT_ESHAPE beyond them). */
+#define DDT_MAX_TOPK 32           /* K                                         */
+#define DDT_MAX_DEPTH 64          /* D                                         */
+#define DDT_MAX_NODES 128         /* N = budget + 1                            */
+
+/* Human-readable name of a status code (static string). */
+const char* ddtree_status_string(int status);
+
+/* Text of the last CUDA error seen by a call that returned DDT_ECUDA on this
+ * host thread ("" if none). */
+const char* ddtree_last_error(void);
+
+/*
+ * ddtree_build - best-first draft tree from the per-depth top-k.
+ *
+ * [Arch] Section 1 (The Five-Step Flow of DDTree), steps 2-3: a heap keyed by
+ * cumulative log-prob; pop the best node and add it; push its best child and
+ * its next sibling; stop after `budget` nodes (budget + 1 with the root). The
+ * mask lets each node see its ancestors and itself (and, implicitly, the whole
+ * context). [Branch] Context section: the cap K bounds the children of a node;
+ * Hypothesis 3: a node at depth d sits at position ctx_len + d, so siblings
+ * share a position; Hypothesis 4: every node of depth d takes its children
+ * from the same depth-(d+1) top-k.
+ *
+ * Inputs
+ *   topk_logp  fp32  [B, D, K]  log-probs of depth d+1's top-K, sorted
+ *                               descending along K (d = 0..D-1)
+ *   topk_tok   int32 [B, D, K]  their token ids (distinct along K)
+ *   root_tok   int32 [B]        the anchor token (tree row 0)
+ *   ctx_len    int32 [B]        tokens already in the KV cache
+ * Outputs, [B, N] unless stated; row 0 is the root, rows are in pop order so a
+ * parent always precedes its children; rows >= n_nodes[b] are pads:
+ *   parent       int32   root -1, pad -1
+ *   depth        int32   root 0,  pad -1
+ *   token        int32   root root_tok, pad -1
+ *   rank         int32   rank within its depth's top-k; root 0, pad -1
+ *   pos          int32   ctx_len + depth; pad -1
+ *   score        float64 cumulative log-prob (fp64 sums of the fp32 inputs in
+ *                        path order); root 0, pad -inf
+ *   first_child  int32   first child in index (= rank) order, -1 if none
+ *   next_sibling int32   next child of the same parent, -1 if none
+ *   vis          uint32 [B, N, W]  bit (j % 32) of word j / 32 set iff row j
+ *                        is row i or an ancestor of it; pads all zero
+ *   n_nodes      int32 [B]   1 + nodes chosen (< N only if the candidates run
+ *                        out, e.g. K = 1 and budget > D)
+ * Ties in score go to the earlier push; a popped node pushes its child before
+ * its sibling. 1 <= K <= 32, 1 <= D <= 64, 0 <= budget <= 127.
+ * Device errors: ctx_len < 0 sets DDT_DEV_BAD_CTX (pos is still written).
+ */
+int ddtree_build(const float* topk_logp, const int32_t* topk_tok,
+                 const int32_t* root_tok, const int32_t* ctx_len,
+                 int B, int D, int K, int budget,
+                 int32_t* parent, int32_t* depth, int32_t* token, int32_t* rank,
+                 int32_t* pos, double* score, int32_t* first_child,
+                 int32_t* next_sibling, uint32_t* vis, int32_t* n_nodes,
+                 int32_t* dev_status, void* stream);
+
+/*
+ * tree_verify_attn - attention of all tree rows in one pass.
+ *
+ * [Arch] Section 1, step 4: all budget+1 nodes go through the target at once
+ * with the tree mask; Section 2 (Context Loading): every node sees the whole
+ * prefix, whose KV is read once and shared by all nodes. [Pivot] The Design
+ * Constraint (Load Contexts Once).
+ *
+ * For request b, row i < n_nodes[b] and query head h (kv head h / (Hq/Hkv)):
+ *   out[b,i,h,:] = softmax_j(scale * q[b,i,h,:] . k_j) v_j
+ * over the ctx_len[b] context keys (all visible) followed by the tree keys j
+ * whose bit is set in vis[b,i,:]. Rows i >= n_nodes[b] get zeros.
+ *
+ * Inputs
+ *   q           bf16  [B, N, Hq, Dh]
+ *   k_tree      bf16  [B, N, Hkv, Dh]   K of the tree rows (row 0 = root)
+ *   v_tree      bf16  [B, N, Hkv, Dh]
+ *   k_cache     bf16  [num_pages, page_size, Hkv, Dh]  paged context K
+ *   v_cache     bf16  [num_pages, page_size, Hkv, Dh]
+ *   page_table  int32 [B, max_pages]  token t of request b is slot
+ *               t % page_size of page page_table[b, t / page_size]; only
+ *               the first ceil(ctx_len[b] / page_size) entries are read
+ *   ctx_len     int32 [B]
+ *   vis         uint32 [B, N, W]   as written by ddtree_build
+ *   n_nodes     int32 [B]
+ * Outputs
+ *   out         bf16  [B, N, Hq, Dh]
+ *   lse         fp32  [B, N, Hq] (nullable): natural-log softmax denominator
+ *               (log-sum-exp of the scaled scores); -inf for pad rows
+ * Workspace: `workspace` (device, >= tree_verify_attn_workspace_size(...)
+ * bytes, 256-byte aligned) holds split-KV partial results; its contents on
+ * entry do not matter. Slots of a page at or beyond ctx_len[b] are never used
+ * (their values may be anything, NaN included).
+ * Supported: Dh in {64, 128}; 1 <= Hkv <= Hq, Hq % Hkv == 0; N <= 128;
+ * page_size a multiple of 16 in [16, 1024]; ctx_len[b] <= max_pages * page_size.
+ * Device errors: DDT_DEV_BAD_PAGE (that page's slots are read as zeros),
+ * DDT_DEV_BAD_CTX (the request's rows are zeros).
+ */
+int tree_verify_attn(const ddtree_bf16* q, const ddtree_bf16* k_tree,
+                     const ddtree_bf16* v_tree, const ddtree_bf16* k_cache,
+                     const ddtree_bf16* v_cache, int num_pages, int page_size,
+                     const int32_t* page_table, int max_pages,
+                     const int32_t* ctx_len, const uint32_t* vis,
+                     const int32_t* n_nodes, int B, int N, int Hq, int Hkv, int Dh,
+                     float scale, ddtree_bf16* out, float* lse, void* workspace,
+                     size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* Bytes of workspace tree_verify_attn needs for these sizes when every
+ * context is at most max_ctx tokens (max_ctx = max_pages * page_size covers
+ * any page table). Returns 0 for unsupported sizes. */
+size_t tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int Dh,
+                                       int max_ctx);
+
+/*
+ * ddtree_accept_greedy - the greedy verify walk.
+ *
+ * [Arch] Section 1, step 5: from the root, follow the target's argmax at the
+ * current node into the child carrying that token; stop when no child
+ * matches; the accepted chain plus one bonus token (the argmax at the last
+ * node) is committed. [Verify] Context section: on a chain this is the linear
+ * rule (draft i is accepted while the argmax at position i-1 equals it).
+ *
+ * Inputs
+ *   logits        fp32 [B, N, V]  row u = target prediction for the token
+ *                                 after node u; only rows on the walk are read
+ *   token, first_child, next_sibling  int32 [B, N]  from ddtree_build
+ *   n_nodes       int32 [B]
+ * Outputs
+ *   accept_len    int32 [B]       accepted draft tokens (bonus excluded)
+ *   out_tokens    int32 [B, D+1]  accepted tokens then the bonus; -1 after
+ *   out_nodes     int32 [B, D+1]  row 0 then the accepted rows; -1 after
+ *   bonus         int32 [B]
+ * Argmax ties go to the lowest index; NaN ranks below every number (an
+ * all-NaN row gives 0). Device errors: DDT_DEV_BAD_TREE (walk stops).
+ */
+int ddtree_accept_greedy(const float* logits, int V, const int32_t* token,
+                         const int32_t* first_child, const int32_t* next_sibling,
+                         const int32_t* n_nodes, int B, int N, int D,
+                         int32_t* accept_len, int32_t* out_tokens,
+                         int32_t* out_nodes, int32_t* bonus,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * ddtree_accept_sample - verify at temperature by recursive rejection
+ * sampling over siblings.
+ *
+ * [Arch] Section 3 (Temperature Support), tree case: at each node reject-
+ * sample the children in turn, descend on an acceptance, and once all are
+ * rejected draw the bonus from the residual and stop. [Verify] Path B and
+ * item 3 of the knowledge list: target q = softmax(logits / T), accept with
+ * min(1, q/p), renormalise q on rejection. A DDTree child is a deterministic
+ * top-k token (a point-mass proposal), so child j of a node, token x_j, is
+ * accepted when u_j * (1 - sum_{i<j} q(x_i)) < q(x_j); the bonus is sampled
+ * from q with the node's children removed (Gumbel-max). Emitted tokens are
+ * distributed exactly as the target.
+ *
+ * Inputs: as ddtree_accept_greedy, plus
+ *   temperature  fp32   [B]   T > 0 per request
+ *   seed         uint64 [B]   Philox key per request
+ *   philox_offset             advance per decoding step; < 2^56
+ * Randomness: Philox4x32-10 with key (seed lo32, seed hi32) and counter
+ * (purpose | (offset >> 32) << 8, node, index, offset lo32): purpose 0 =
+ * child test (index = child slot, word 0), purpose 1 = Gumbel noise for vocab
+ * entry v (index = v >> 2, word v & 3); uniform = ((w >> 8) + 0.5) * 2^-24.
+ * Outputs: as ddtree_accept_greedy. Logits must be finite.
+ * Device errors: DDT_DEV_BAD_TEMPERATURE (that request emits nothing:
+ * accept_len 0, bonus -1), DDT_DEV_BAD_TREE.
+ */
+int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
+                         const int32_t* first_child, const int32_t* next_sibling,
+                         const int32_t* n_nodes, int B, int N, int D,
+                         const float* temperature, const uint64_t* seed,
+                         uint64_t philox_offset, int32_t* accept_len,
+                         int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
+                         int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDTREE_H */

@@ -86,6 +86,10 @@ def draft_topk(draft_logits: np.ndarray, K: int):
 # a1: best-first tree build, visibility and positions
 # ----------------------------------------------------------------------------
 
+def _nan_low(s: float) -> float:
+    return -math.inf if s != s else s
+
+
 @dataclass
 class Tree:
     """Tree arrays for a batch; N = budget + 1 rows per request."""
@@ -120,13 +124,13 @@ def build_tree(topk_logp: np.ndarray, topk_tok: np.ndarray, root_tok: np.ndarray
     * heap order: larger score first, then the earlier push; the child is
       pushed before the sibling;
     * the depth never exceeds D; if the heap empties first, n_nodes < N and the
-      remaining rows are pads.
+      remaining rows are pads;
+    * a NaN score (from a NaN log-prob) ranks as -inf.
     """
     lp = np.asarray(topk_logp, dtype=np.float32)
     tk = np.asarray(topk_tok, dtype=np.int32)
     B, D, K = lp.shape
     N = budget + 1
-    W = (N + 31) // 32
     parent = np.full((B, N), -1, np.int32)
     depth = np.full((B, N), -1, np.int32)
     token = np.full((B, N), -1, np.int32)
@@ -142,7 +146,7 @@ def build_tree(topk_logp: np.ndarray, topk_tok: np.ndarray, root_tok: np.ndarray
         heap = []
         seq = 0
         if D >= 1 and K >= 1 and budget >= 1:
-            heapq.heappush(heap, (-(0.0 + float(lp[b, 0, 0])), seq, 1, 0, 0))
+            heapq.heappush(heap, (-_nan_low(0.0 + float(lp[b, 0, 0])), seq, 1, 0, 0))
             seq += 1
         count = 0
         while count < budget and heap:
@@ -155,10 +159,10 @@ def build_tree(topk_logp: np.ndarray, topk_tok: np.ndarray, root_tok: np.ndarray
             token[b, i] = int(tk[b, d - 1, r])
             score[b, i] = -neg
             if d < D:   # best child: rank 0 at depth d+1
-                heapq.heappush(heap, (-(score[b, i] + float(lp[b, d, 0])), seq, d + 1, 0, i))
+                heapq.heappush(heap, (-_nan_low(score[b, i] + float(lp[b, d, 0])), seq, d + 1, 0, i))
                 seq += 1
             if r + 1 < K:   # next sibling: same parent, rank r+1
-                heapq.heappush(heap, (-(score[b, p] + float(lp[b, d - 1, r + 1])), seq, d, r + 1, p))
+                heapq.heappush(heap, (-_nan_low(score[b, p] + float(lp[b, d - 1, r + 1])), seq, d, r + 1, p))
                 seq += 1
         n_nodes[b] = count + 1
         for i in range(count + 1):
@@ -552,12 +556,18 @@ def accept_sample(logits: np.ndarray, tree: Tree, D: int, temperature: np.ndarra
             w = stacked[(vidx & np.uint64(3)).astype(np.int64), np.arange(V)]
             g = -np.log(-np.log(to_uniform(w)))
             pert = row + g
+            allowed = np.ones(V, bool)
             for c in kids:
-                pert[int(tree.token[b, c])] = -np.inf
-            best = int(np.argmax(pert))
-            top2 = np.partition(pert, -2)[-2:] if V >= 2 else np.array([-np.inf, pert[0]])
-            margin[b] = min(margin[b], float(top2[1] - top2[0]))
-            bonus[b] = best
+                allowed[int(tree.token[b, c])] = False
+            cand = np.nonzero(allowed)[0]
+            if cand.size == 0:      # every token is a child: nothing left to draw
+                bonus[b] = -1
+            else:
+                best = int(cand[np.argmax(pert[cand])])
+                if cand.size >= 2:
+                    top2 = np.partition(pert[cand], -2)[-2:]
+                    margin[b] = min(margin[b], float(top2[1] - top2[0]))
+                bonus[b] = best
             break
         acc[b] = len(path)
         nodes[b, 0] = 0

@@ -1,0 +1,128 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and
+rejects bad arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ddtree.h")
+
+from tree_speculative_decoding_ddtree_gb300 import _build  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = _build.build()
+    import tree_speculative_decoding_ddtree_gb300 as dd
+    return dd.load_library(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("ddtree_build", "tree_verify_attn", "ddtree_accept_greedy", "ddtree_accept_sample"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -6):
+        assert lib.ddtree_status_string(code)
+    assert lib.ddtree_last_error() == b""
+
+
+FAKE = 4096   # an aligned non-null address; host checks fail before any launch
+
+
+def build_args(B=2, D=3, K=4, budget=5, null=None):
+    ptrs = [FAKE] * 4 + [FAKE] * 10
+    if null is not None:
+        ptrs[null] = 0
+    return ptrs[:4] + [B, D, K, budget] + ptrs[4:] + [0, 0]
+
+
+@pytest.mark.parametrize("D,K,budget,code", [(3, 0, 5, -2), (3, 33, 5, -2), (0, 4, 5, -2),
+                                             (65, 4, 5, -2), (3, 4, 128, -2), (3, 4, -1, -2)])
+def test_build_rejects_shapes(lib, D, K, budget, code):
+    assert lib.ddtree_build(*build_args(D=D, K=K, budget=budget)) == code
+
+
+@pytest.mark.parametrize("null", range(14))
+def test_build_rejects_null_pointers(lib, null):
+    assert lib.ddtree_build(*build_args(null=null)) == -1
+
+
+def test_build_empty_batch_is_a_noop(lib):
+    assert lib.ddtree_build(*build_args(B=0, null=3)) == 0
+
+
+def attn_args(**kw):
+    a = dict(q=FAKE, kt=FAKE, vt=FAKE, kc=FAKE, vc=FAKE, num_pages=10, page_size=64, table=FAKE,
+             max_pages=256, ctx=FAKE, vis=FAKE, nn=FAKE, B=2, N=33, Hq=64, Hkv=8, Dh=128, scale=0.1,
+             out=FAKE, lse=0, ws=FAKE, ws_bytes=1 << 40, status=0, stream=0)
+    a.update(kw)
+    return [a[k] for k in ("q", "kt", "vt", "kc", "vc", "num_pages", "page_size", "table",
+                           "max_pages", "ctx", "vis", "nn", "B", "N", "Hq", "Hkv", "Dh", "scale",
+                           "out", "lse", "ws", "ws_bytes", "status", "stream")]
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Dh=96), -2), (dict(Hq=60), -2), (dict(N=129), -2), (dict(N=0), -2),
+    (dict(page_size=8), -2), (dict(page_size=100), -2), (dict(num_pages=0), -2),
+    (dict(scale=float("nan")), -1), (dict(q=0), -1), (dict(out=0), -1), (dict(vis=0), -1),
+    (dict(q=FAKE + 8), -1), (dict(ws=0), -6), (dict(ws_bytes=16), -6), (dict(ws=FAKE + 16), -6),
+    (dict(B=-1), -1), (dict(B=0, q=0), 0),
+])
+def test_attn_rejects_bad_arguments(lib, kw, code):
+    assert lib.tree_verify_attn(*attn_args(**kw)) == code
+
+
+def test_workspace_size(lib):
+    assert lib.tree_verify_attn_workspace_size(16, 33, 64, 8, 128, 16384) > 0
+    assert lib.tree_verify_attn_workspace_size(16, 33, 64, 8, 96, 16384) == 0
+    # a short context needs no split and no workspace
+    assert lib.tree_verify_attn_workspace_size(1, 33, 64, 8, 128, 64) == 0
+    small = lib.tree_verify_attn_workspace_size(1, 33, 64, 8, 128, 4096)
+    big = lib.tree_verify_attn_workspace_size(1, 33, 64, 8, 128, 32768)
+    assert 0 < small <= big
+
+
+def walk_args(sample=False, **kw):
+    a = dict(logits=FAKE, V=100, token=FAKE, fc=FAKE, ns=FAKE, nn=FAKE, B=2, N=33, D=8,
+             acc=FAKE, toks=FAKE, nodes=FAKE, bonus=FAKE, status=0, stream=0,
+             temp=FAKE, seed=FAKE, offset=0)
+    a.update(kw)
+    head = [a[k] for k in ("logits", "V", "token", "fc", "ns", "nn", "B", "N", "D")]
+    tail = [a[k] for k in ("acc", "toks", "nodes", "bonus", "status", "stream")]
+    if sample:
+        return head + [a["temp"], a["seed"], a["offset"]] + tail
+    return head + tail
+
+
+@pytest.mark.parametrize("kw,code", [(dict(V=0), -1), (dict(N=200), -2), (dict(D=0), -2),
+                                     (dict(logits=0), -1), (dict(bonus=0), -1), (dict(B=0, logits=0), 0)])
+def test_walks_reject_bad_arguments(lib, kw, code):
+    assert lib.ddtree_accept_greedy(*walk_args(**kw)) == code
+    assert lib.ddtree_accept_sample(*walk_args(sample=True, **kw)) == code
+
+
+def test_sample_rejects_missing_rng_inputs_and_large_offset(lib):
+    assert lib.ddtree_accept_sample(*walk_args(sample=True, temp=0)) == -1
+    assert lib.ddtree_accept_sample(*walk_args(sample=True, seed=0)) == -1
+    assert lib.ddtree_accept_sample(*walk_args(sample=True, offset=1 << 56)) == -1

@@ -1,0 +1,254 @@
+"""DDTree tree-verify step on one GB300: thin Python binding of ``libddtree.so``.
+
+The four calls of the C ABI (``include/ddtree.h``) are exposed under the same
+names. This module only marshals arguments: it checks that tensors are CUDA,
+contiguous and of the right dtype and shape, passes their device pointers and
+the current stream, and raises :class:`DDTreeError` on a non-zero status. All
+computation runs in the library's CUDA kernels; there is no fallback. PyTorch
+serves for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "DDTreeError", "load_library", "library_path", "ddtree_build", "tree_verify_attn",
+    "tree_verify_attn_workspace_size", "ddtree_accept_greedy", "ddtree_accept_sample",
+    "TreeBuffers", "alloc_tree", "DEV_ERRORS",
+]
+
+DEV_ERRORS = {
+    1: "DDT_DEV_BAD_PAGE", 2: "DDT_DEV_BAD_CTX", 4: "DDT_DEV_BAD_TREE",
+    8: "DDT_DEV_BAD_TEMPERATURE", 16: "DDT_DEV_BAD_TOKEN",
+}
+
+_lib = None
+
+
+class DDTreeError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({detail})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: Optional[str] = None):
+    """Load ``libddtree.so`` (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"DDTree CUDA library not found at {p}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (no CPU fallback exists)")
+    lib = ctypes.CDLL(p)
+    P, I, F, Z, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+    lib.ddtree_status_string.restype = ctypes.c_char_p
+    lib.ddtree_status_string.argtypes = [I]
+    lib.ddtree_last_error.restype = ctypes.c_char_p
+    lib.ddtree_last_error.argtypes = []
+    lib.ddtree_build.restype = I
+    lib.ddtree_build.argtypes = [P] * 4 + [I] * 4 + [P] * 10 + [P, P]
+    lib.tree_verify_attn.restype = I
+    lib.tree_verify_attn.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P, I, I, I, I, I, F,
+                                     P, P, P, Z, P, P]
+    lib.tree_verify_attn_workspace_size.restype = Z
+    lib.tree_verify_attn_workspace_size.argtypes = [I, I, I, I, I, I]
+    lib.ddtree_accept_greedy.restype = I
+    lib.ddtree_accept_greedy.argtypes = [P, I, P, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.ddtree_accept_sample.restype = I
+    lib.ddtree_accept_sample.argtypes = [P, I, P, P, P, P, I, I, I, P, P, U64, P, P, P, P, P, P]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        lib = load_library()
+        detail = lib.ddtree_status_string(status).decode()
+        if status == -3:
+            detail += ": " + lib.ddtree_last_error().decode()
+        raise DDTreeError(status, where, detail)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype, name: str, shape=None) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class TreeBuffers:
+    """Device outputs of ``ddtree_build`` for B requests and N = budget + 1 rows."""
+
+    def __init__(self, B: int, N: int, device):
+        W = (N + 31) // 32
+        i32 = dict(dtype=torch.int32, device=device)
+        self.B, self.N, self.W = B, N, W
+        self.parent = torch.empty((B, N), **i32)
+        self.depth = torch.empty((B, N), **i32)
+        self.token = torch.empty((B, N), **i32)
+        self.rank = torch.empty((B, N), **i32)
+        self.pos = torch.empty((B, N), **i32)
+        self.score = torch.empty((B, N), dtype=torch.float64, device=device)
+        self.first_child = torch.empty((B, N), **i32)
+        self.next_sibling = torch.empty((B, N), **i32)
+        self.vis = torch.empty((B, N, W), dtype=torch.int32, device=device)  # uint32 bits
+        self.n_nodes = torch.empty((B,), **i32)
+
+
+def alloc_tree(B: int, N: int, device="cuda") -> TreeBuffers:
+    return TreeBuffers(B, N, device)
+
+
+def ddtree_build(topk_logp: torch.Tensor, topk_tok: torch.Tensor, root_tok: torch.Tensor,
+                 ctx_len: torch.Tensor, budget: int, out: Optional[TreeBuffers] = None,
+                 dev_status: Optional[torch.Tensor] = None, stream=None) -> TreeBuffers:
+    """Best-first tree from per-depth top-k (see ``ddtree_build`` in include/ddtree.h)."""
+    lib = load_library()
+    B, D, K = topk_logp.shape
+    N = budget + 1
+    if out is None:
+        out = TreeBuffers(B, N, topk_logp.device)
+    st = lib.ddtree_build(
+        _ptr(topk_logp, torch.float32, "topk_logp", (B, D, K)),
+        _ptr(topk_tok, torch.int32, "topk_tok", (B, D, K)),
+        _ptr(root_tok, torch.int32, "root_tok", (B,)),
+        _ptr(ctx_len, torch.int32, "ctx_len", (B,)),
+        B, D, K, budget,
+        _ptr(out.parent, torch.int32, "parent", (B, N)), _ptr(out.depth, torch.int32, "depth", (B, N)),
+        _ptr(out.token, torch.int32, "token", (B, N)), _ptr(out.rank, torch.int32, "rank", (B, N)),
+        _ptr(out.pos, torch.int32, "pos", (B, N)), _ptr(out.score, torch.float64, "score", (B, N)),
+        _ptr(out.first_child, torch.int32, "first_child", (B, N)),
+        _ptr(out.next_sibling, torch.int32, "next_sibling", (B, N)),
+        _ptr(out.vis, torch.int32, "vis", (B, N, (N + 31) // 32)),
+        _ptr(out.n_nodes, torch.int32, "n_nodes", (B,)),
+        _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
+    _check(st, "ddtree_build")
+    return out
+
+
+def tree_verify_attn_workspace_size(B: int, N: int, Hq: int, Hkv: int, Dh: int, max_ctx: int) -> int:
+    return int(load_library().tree_verify_attn_workspace_size(B, N, Hq, Hkv, Dh, max_ctx))
+
+
+def tree_verify_attn(q: torch.Tensor, k_tree: torch.Tensor, v_tree: torch.Tensor,
+                     k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+                     ctx_len: torch.Tensor, vis: torch.Tensor, n_nodes: torch.Tensor,
+                     scale: float, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Tree-verify attention (see ``tree_verify_attn`` in include/ddtree.h).
+
+    ``q`` is bf16 ``[B, N, Hq, Dh]``; ``k_cache``/``v_cache`` are bf16
+    ``[num_pages, page_size, Hkv, Dh]``. A workspace of the required size is
+    allocated here when none is given.
+    """
+    lib = load_library()
+    B, N, Hq, Dh = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    max_pages = page_table.shape[1]
+    W = (N + 31) // 32
+    if out is None:
+        out = torch.empty_like(q)
+    need = tree_verify_attn_workspace_size(B, N, Hq, Hkv, Dh, max_pages * page_size)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.tree_verify_attn(
+        _ptr(q, torch.bfloat16, "q", (B, N, Hq, Dh)),
+        _ptr(k_tree, torch.bfloat16, "k_tree", (B, N, Hkv, Dh)),
+        _ptr(v_tree, torch.bfloat16, "v_tree", (B, N, Hkv, Dh)),
+        _ptr(k_cache, torch.bfloat16, "k_cache", (num_pages, page_size, Hkv, Dh)),
+        _ptr(v_cache, torch.bfloat16, "v_cache", (num_pages, page_size, Hkv, Dh)),
+        num_pages, page_size,
+        _ptr(page_table, torch.int32, "page_table", (B, max_pages)), max_pages,
+        _ptr(ctx_len, torch.int32, "ctx_len", (B,)),
+        _ptr(vis, torch.int32, "vis", (B, N, W)),
+        _ptr(n_nodes, torch.int32, "n_nodes", (B,)),
+        B, N, Hq, Hkv, Dh, float(scale),
+        _ptr(out, torch.bfloat16, "out", (B, N, Hq, Dh)),
+        _ptr(lse, torch.float32, "lse", (B, N, Hq)),
+        _ptr(workspace, torch.uint8, "workspace") if workspace is not None else 0,
+        workspace.numel() if workspace is not None else 0,
+        _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
+    _check(st, "tree_verify_attn")
+    return out
+
+
+def _walk_outputs(B, D, device, out):
+    if out is not None:
+        return out
+    i32 = dict(dtype=torch.int32, device=device)
+    return dict(accept_len=torch.empty(B, **i32), out_tokens=torch.empty((B, D + 1), **i32),
+                out_nodes=torch.empty((B, D + 1), **i32), bonus=torch.empty(B, **i32))
+
+
+def ddtree_accept_greedy(logits: torch.Tensor, tree: TreeBuffers, D: int, out=None,
+                         dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Greedy verify walk (see ``ddtree_accept_greedy`` in include/ddtree.h)."""
+    lib = load_library()
+    B, N, V = logits.shape
+    o = _walk_outputs(B, D, logits.device, out)
+    st = lib.ddtree_accept_greedy(
+        _ptr(logits, torch.float32, "logits", (B, N, V)), V,
+        _ptr(tree.token, torch.int32, "token", (B, N)),
+        _ptr(tree.first_child, torch.int32, "first_child", (B, N)),
+        _ptr(tree.next_sibling, torch.int32, "next_sibling", (B, N)),
+        _ptr(tree.n_nodes, torch.int32, "n_nodes", (B,)), B, N, D,
+        _ptr(o["accept_len"], torch.int32, "accept_len", (B,)),
+        _ptr(o["out_tokens"], torch.int32, "out_tokens", (B, D + 1)),
+        _ptr(o["out_nodes"], torch.int32, "out_nodes", (B, D + 1)),
+        _ptr(o["bonus"], torch.int32, "bonus", (B,)),
+        _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
+    _check(st, "ddtree_accept_greedy")
+    return o
+
+
+def ddtree_accept_sample(logits: torch.Tensor, tree: TreeBuffers, D: int,
+                         temperature: torch.Tensor, seed: torch.Tensor, philox_offset: int,
+                         out=None, dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Temperature verify walk (see ``ddtree_accept_sample`` in include/ddtree.h).
+
+    ``seed`` is int64 on the device, read as uint64 bits.
+    """
+    lib = load_library()
+    B, N, V = logits.shape
+    o = _walk_outputs(B, D, logits.device, out)
+    st = lib.ddtree_accept_sample(
+        _ptr(logits, torch.float32, "logits", (B, N, V)), V,
+        _ptr(tree.token, torch.int32, "token", (B, N)),
+        _ptr(tree.first_child, torch.int32, "first_child", (B, N)),
+        _ptr(tree.next_sibling, torch.int32, "next_sibling", (B, N)),
+        _ptr(tree.n_nodes, torch.int32, "n_nodes", (B,)), B, N, D,
+        _ptr(temperature, torch.float32, "temperature", (B,)),
+        _ptr(seed, torch.int64, "seed", (B,)), int(philox_offset),
+        _ptr(o["accept_len"], torch.int32, "accept_len", (B,)),
+        _ptr(o["out_tokens"], torch.int32, "out_tokens", (B, D + 1)),
+        _ptr(o["out_nodes"], torch.int32, "out_nodes", (B, D + 1)),
+        _ptr(o["bonus"], torch.int32, "bonus", (B,)),
+        _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
+    _check(st, "ddtree_accept_sample")
+    return o

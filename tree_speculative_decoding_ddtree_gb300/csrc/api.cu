@@ -1,0 +1,199 @@
+// C ABI of the DDTree verify step: host-side argument checks, then launches.
+// Nothing here allocates or synchronises; every call is stream-ordered.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "attn.cuh"
+#include "common.cuh"
+
+namespace ddt {
+cudaError_t launch_build(const float*, const int32_t*, const int32_t*, const int32_t*, int, int,
+                         int, int, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, double*,
+                         int32_t*, int32_t*, uint32_t*, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_accept_greedy(const float*, int, const int32_t*, const int32_t*,
+                                 const int32_t*, const int32_t*, int, int, int, int32_t*,
+                                 int32_t*, int32_t*, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_accept_sample(const float*, int, const int32_t*, const int32_t*,
+                                 const int32_t*, const int32_t*, int, int, int, const float*,
+                                 const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*,
+                                 int32_t*, int32_t*, cudaStream_t);
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+int cuda_fail(cudaError_t e) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return DDT_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kPlanSMs = 152;        // GB300 SM count used to size the split-KV grid
+constexpr int kPlanWaves = 4;        // target CTAs per SM over a full-length batch
+constexpr int kKeyTile = 64;
+
+struct AttnPlan {
+    int R, rows_per_group, n_groups, tiles_per_chunk, max_chunks;
+    size_t ws_o_bytes, ws_ml_bytes;
+};
+
+bool plan_attn(int B, int N, int Hq, int Hkv, int Dh, long long max_ctx, AttnPlan* pl) {
+    if (B < 1 || N < 1 || N > DDT_MAX_NODES || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 ||
+        (Dh != 64 && Dh != 128) || max_ctx < 0 || max_ctx > (1ll << 30))
+        return false;
+    const long long R = static_cast<long long>(N) * (Hq / Hkv);
+    if (R > (1 << 20)) return false;
+    pl->R = static_cast<int>(R);
+    pl->n_groups = static_cast<int>((R + kMaxRowsPerCta - 1) / kMaxRowsPerCta);
+    // spread rows evenly over the groups, in whole 16-row blocks
+    const long long per = (R + pl->n_groups - 1) / pl->n_groups;
+    pl->rows_per_group = static_cast<int>((per + 15) / 16 * 16);
+    if (pl->rows_per_group > kMaxRowsPerCta) pl->rows_per_group = kMaxRowsPerCta;
+    const long long tiles = (max_ctx + kKeyTile - 1) / kKeyTile;
+    const long long total = static_cast<long long>(B) * Hkv * pl->n_groups * (tiles > 0 ? tiles : 1);
+    long long tpc = (total + kPlanSMs * kPlanWaves - 1) / (kPlanSMs * kPlanWaves);
+    if (tpc < 4) tpc = 4;
+    pl->tiles_per_chunk = static_cast<int>(tpc);
+    pl->max_chunks = tiles > 0 ? static_cast<int>((tiles + tpc - 1) / tpc) : 1;
+    const size_t slots = static_cast<size_t>(B) * Hkv * pl->max_chunks * R;
+    pl->ws_o_bytes = pl->max_chunks > 1 ? (slots * Dh * sizeof(float) + 255) / 256 * 256 : 0;
+    pl->ws_ml_bytes = pl->max_chunks > 1 ? (slots * sizeof(float2) + 255) / 256 * 256 : 0;
+    return true;
+}
+
+}  // namespace
+}  // namespace ddt
+
+using namespace ddt;
+
+extern "C" {
+
+const char* ddtree_status_string(int status) {
+    switch (status) {
+        case DDT_OK: return "DDT_OK";
+        case DDT_EINVAL: return "DDT_EINVAL: null pointer or bad scalar argument";
+        case DDT_ESHAPE: return "DDT_ESHAPE: sizes outside the supported range";
+        case DDT_ECUDA: return "DDT_ECUDA: a CUDA call or launch failed";
+        case DDT_ETIMEOUT: return "DDT_ETIMEOUT: a bounded device wait gave up";
+        case DDT_EWORKSPACE: return "DDT_EWORKSPACE: workspace missing or too small";
+        default: return "unknown ddtree status";
+    }
+}
+
+const char* ddtree_last_error(void) { return g_last_error; }
+
+int ddtree_build(const float* topk_logp, const int32_t* topk_tok, const int32_t* root_tok,
+                 const int32_t* ctx_len, int B, int D, int K, int budget, int32_t* parent,
+                 int32_t* depth, int32_t* token, int32_t* rank, int32_t* pos, double* score,
+                 int32_t* first_child, int32_t* next_sibling, uint32_t* vis, int32_t* n_nodes,
+                 int32_t* dev_status, void* stream) {
+    if (B < 0) return DDT_EINVAL;
+    if (K < 1 || K > DDT_MAX_TOPK || D < 1 || D > DDT_MAX_DEPTH || budget < 0 ||
+        budget + 1 > DDT_MAX_NODES)
+        return DDT_ESHAPE;
+    if (B == 0) return DDT_OK;
+    if (!topk_logp || !topk_tok || !root_tok || !ctx_len || !parent || !depth || !token ||
+        !rank || !pos || !score || !first_child || !next_sibling || !vis || !n_nodes)
+        return DDT_EINVAL;
+    cudaError_t e = launch_build(topk_logp, topk_tok, root_tok, ctx_len, B, D, K, budget, parent,
+                                 depth, token, rank, pos, score, first_child, next_sibling, vis,
+                                 n_nodes, dev_status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+size_t tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int Dh, int max_ctx) {
+    AttnPlan pl;
+    if (!plan_attn(B, N, Hq, Hkv, Dh, max_ctx, &pl)) return 0;
+    return pl.ws_o_bytes + pl.ws_ml_bytes;
+}
+
+int tree_verify_attn(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtree_bf16* v_tree,
+                     const ddtree_bf16* k_cache, const ddtree_bf16* v_cache, int num_pages,
+                     int page_size, const int32_t* page_table, int max_pages,
+                     const int32_t* ctx_len, const uint32_t* vis, const int32_t* n_nodes,
+                     int B, int N, int Hq, int Hkv, int Dh, float scale, ddtree_bf16* out,
+                     float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream) {
+    if (B < 0 || !std::isfinite(scale)) return DDT_EINVAL;
+    if (page_size < 16 || page_size > 1024 || page_size % 16 != 0 || num_pages < 1 ||
+        max_pages < 1)
+        return DDT_ESHAPE;
+    const long long max_ctx = static_cast<long long>(max_pages) * page_size;
+    AttnPlan pl;
+    if (!plan_attn(B > 0 ? B : 1, N, Hq, Hkv, Dh, max_ctx, &pl)) return DDT_ESHAPE;
+    if (B == 0) return DDT_OK;
+    if (!q || !k_tree || !v_tree || !k_cache || !v_cache || !page_table || !ctx_len || !vis ||
+        !n_nodes || !out)
+        return DDT_EINVAL;
+    if (!aligned16(q) || !aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_cache) ||
+        !aligned16(v_cache) || !aligned16(out))
+        return DDT_EINVAL;
+    const size_t need = pl.ws_o_bytes + pl.ws_ml_bytes;
+    if (need > 0 && (!workspace || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return DDT_EWORKSPACE;
+    AttnParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q; p.k_tree = k_tree; p.v_tree = v_tree; p.k_cache = k_cache; p.v_cache = v_cache;
+    p.page_table = page_table; p.ctx_len = ctx_len; p.vis = vis; p.n_nodes = n_nodes;
+    p.out = out; p.lse = lse; p.dev_status = dev_status;
+    p.ws_o = need ? static_cast<float*>(workspace) : nullptr;
+    p.ws_ml = need ? reinterpret_cast<float2*>(static_cast<char*>(workspace) + pl.ws_o_bytes) : nullptr;
+    p.num_pages = num_pages; p.page_size = page_size; p.max_pages = max_pages;
+    p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.Dh = Dh; p.G = Hq / Hkv; p.W = (N + 31) / 32;
+    p.R = pl.R; p.rows_per_group = pl.rows_per_group; p.n_groups = pl.n_groups;
+    p.tiles_per_chunk = pl.tiles_per_chunk; p.max_chunks = pl.max_chunks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = launch_attn_mma(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+static int check_walk_args(const float* logits, int V, const int32_t* token,
+                           const int32_t* first_child, const int32_t* next_sibling,
+                           const int32_t* n_nodes, int B, int N, int D, int32_t* accept_len,
+                           int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus) {
+    if (B < 0 || V < 1) return DDT_EINVAL;
+    if (N < 1 || N > DDT_MAX_NODES || D < 1 || D > DDT_MAX_DEPTH) return DDT_ESHAPE;
+    if (B == 0) return DDT_OK;
+    if (!logits || !token || !first_child || !next_sibling || !n_nodes || !accept_len ||
+        !out_tokens || !out_nodes || !bonus)
+        return DDT_EINVAL;
+    return DDT_OK;
+}
+
+int ddtree_accept_greedy(const float* logits, int V, const int32_t* token,
+                         const int32_t* first_child, const int32_t* next_sibling,
+                         const int32_t* n_nodes, int B, int N, int D, int32_t* accept_len,
+                         int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
+                         int32_t* dev_status, void* stream) {
+    int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
+                             accept_len, out_tokens, out_nodes, bonus);
+    if (st != DDT_OK || B == 0) return st;
+    cudaError_t e = launch_accept_greedy(logits, V, token, first_child, next_sibling, n_nodes, B,
+                                         N, D, accept_len, out_tokens, out_nodes, bonus,
+                                         dev_status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
+                         const int32_t* first_child, const int32_t* next_sibling,
+                         const int32_t* n_nodes, int B, int N, int D, const float* temperature,
+                         const uint64_t* seed, uint64_t philox_offset, int32_t* accept_len,
+                         int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
+                         int32_t* dev_status, void* stream) {
+    int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
+                             accept_len, out_tokens, out_nodes, bonus);
+    if (st != DDT_OK || B == 0) return st;
+    if (!temperature || !seed) return DDT_EINVAL;
+    if (philox_offset >> 56) return DDT_EINVAL;
+    cudaError_t e = launch_accept_sample(logits, V, token, first_child, next_sibling, n_nodes, B,
+                                         N, D, temperature, seed, philox_offset, accept_len,
+                                         out_tokens, out_nodes, bonus, dev_status,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+}  // extern "C"
