@@ -71,7 +71,9 @@ enum ddtree_device_error {
     DDT_DEV_BAD_TREE = 4,         /* tree arrays inconsistent (child index out  */
                                   /* of range, walk longer than D, n_nodes > N) */
     DDT_DEV_BAD_TEMPERATURE = 8,  /* temperature <= 0 or not finite             */
-    DDT_DEV_BAD_TOKEN = 16        /* token id outside [0, V)                    */
+    DDT_DEV_BAD_TOKEN = 16,       /* token id outside [0, V)                    */
+    DDT_DEV_TIMEOUT = 32          /* a bounded wait inside a kernel gave up; the */
+                                  /* affected outputs are undefined             */
 };
 
 /* Limits checked on the host (DDT_ESHAPE beyond them). */

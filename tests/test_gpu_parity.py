@@ -176,6 +176,10 @@ def test_attn_tiny_full():
     ([300], 32, 6, 6, 128, 9, 2, 4),                # MHA (G = 1)
     ([5000, 20], 64, 32, 2, 128, 8, 8, 2),          # G = 16: 144 rows
     ([1500], 16, 48, 2, 128, 23, 5, 6),             # G = 24: 576 rows, several row groups
+    ([0, 70, 1000, 3], 64, 64, 8, 128, 32, 8, 8),   # 264 rows: two tensor-core tiles + 8 leftover rows
+    ([129, 4000], 128, 32, 8, 128, 64, 8, 16),      # 260 rows (4 leftover), page 128, two tree tiles
+    ([2000], 32, 16, 2, 128, 32, 4, 6),             # 264 rows, page 32 (two page boxes per key tile)
+    ([6000, 1], 16, 8, 8, 128, 127, 4, 9),          # MHA, N = 128: 128 rows, one tile, page 16
 ])
 def test_attn_ragged_shapes(ctx, page_size, Hq, Hkv, Dh, budget, K, D):
     w = S.Workload(name="ragged", B=len(ctx), D=D, V=300, K=K, budget=budget, Hq=Hq, Hkv=Hkv,

@@ -65,6 +65,7 @@ bool plan_attn(int B, int N, int Hq, int Hkv, int Dh, long long max_ctx, AttnPla
 }
 
 }  // namespace
+
 }  // namespace ddt
 
 using namespace ddt;
@@ -147,7 +148,14 @@ int tree_verify_attn(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtr
     p.R = pl.R; p.rows_per_group = pl.rows_per_group; p.n_groups = pl.n_groups;
     p.tiles_per_chunk = pl.tiles_per_chunk; p.max_chunks = pl.max_chunks;
     p.scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e = launch_attn_mma(p, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (attn_tc_supported(p)) {
+        e = launch_attn_tc(p, st);
+        if (e == cudaSuccess) e = launch_attn_combine(p, st);
+    } else {
+        e = launch_attn_mma(p, st);
+    }
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
 

@@ -31,6 +31,12 @@ struct AttnParams {
     float scale_log2;
 };
 
+// warp-MMA path: any supported shape (split-KV main launch + combine)
 cudaError_t launch_attn_mma(const AttnParams& p, cudaStream_t stream);
+// tensor-core path (tcgen05 + TMA): Dh 128, G dividing 128, R <= 264, one row group
+bool attn_tc_supported(const AttnParams& p);
+cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t stream);
+// merge split-KV partials (no-op launch when every request fits one chunk)
+cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream);
 
 }  // namespace ddt

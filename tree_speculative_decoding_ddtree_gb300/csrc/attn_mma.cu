@@ -209,7 +209,7 @@ attn_mma_kernel(AttnParams p) {
                     const int key = key0 + n * 8 + 2 * (lane & 3) + (e & 1);
                     bool ok;
                     if (is_ctx) ok = key < L;
-                    else ok = key < nn && ((visw[rr][key >> 5] >> (key & 31)) & 1u);
+                    else ok = key < nn && ((pick4(visw[rr], key >> 5) >> (key & 31)) & 1u);
                     s[n][e] = ok ? s[n][e] * p.scale_log2 : -INFINITY;
                 }
             }
@@ -355,16 +355,19 @@ static cudaError_t launch_dh(const AttnParams& p, cudaStream_t stream) {
     attn_mma_kernel<DH><<<grid, 32 * warps, smem, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (p.max_chunks > 1) {
-        const dim3 g2((p.R + 7) / 8, p.Hkv, p.B);
-        attn_combine_kernel<DH><<<g2, 256, 0, stream>>>(p);
-        e = cudaGetLastError();
-    }
-    return e;
+    return launch_attn_combine(p, stream);
 }
 
 cudaError_t launch_attn_mma(const AttnParams& p, cudaStream_t stream) {
     return p.Dh == 128 ? launch_dh<128>(p, stream) : launch_dh<64>(p, stream);
+}
+
+cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream) {
+    if (p.max_chunks <= 1) return cudaSuccess;
+    const dim3 g2((p.R + 7) / 8, p.Hkv, p.B);
+    if (p.Dh == 128) attn_combine_kernel<128><<<g2, 256, 0, stream>>>(p);
+    else attn_combine_kernel<64><<<g2, 256, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace ddt

@@ -1,0 +1,725 @@
+// tree_verify_attn, tensor-core path for sm_103a (tcgen05 + TMA + TMEM).
+//
+// Method: "The Architecture of Speculative Decoding: Dissecting DDTree's
+// Tree-Parallel Evaluation Strategy", Section 1 step 4 (all budget+1 tree
+// rows in one pass under the tree mask) and Section 2 (the context KV is
+// loaded once and shared by all rows); "The Pivot Point", The Design
+// Constraint (load contexts once).
+//
+// One CTA owns every query row of one (request, KV head) and one chunk of its
+// context. Its R = N * G rows (node-major: row r = node r / G, head r % G)
+// are two 128-row tensor-core tiles plus up to 8 leftover rows:
+//
+//   warp 0       TMA producer: Q once, then paged K/V tiles of 64 keys (one
+//                page box per half of the head dim, 128-byte swizzle) into a
+//                4-stage ring; zeroes V rows past the valid keys of a ragged
+//                tile so masked keys contribute exact zeros.
+//   warp 1       allocates TMEM; one lane issues tcgen05.mma:
+//                S_t = Q_t K^T (both K-major in shared memory) and
+//                O_t += P_t V (P from TMEM, V MN-major in shared memory),
+//                ping-ponging the two tiles so the tensor core works on one
+//                tile while the other tile's softmax runs.
+//   warps 4-7,   one thread per row of tile 0 / tile 1 (its TMEM lane): load
+//   warps 8-11   S, mask (context tail, ancestor bitmask on the tree tile),
+//                online softmax in the exp2 domain with a lazy rescale of O
+//                (only when the running max grows by more than 2^8), write P
+//                as bf16 over S in TMEM; final normalisation and store.
+//   warps 12-15  the leftover rows on mma.sync (keys on M, rows on N), reading
+//                the same K/V stages through ldmatrix.
+//
+// TMEM columns: S0/P0 [0,64), S1/P1 [64,128), O0 [128,256), O1 [256,384).
+// Every wait is bounded; a timeout sets DDT_DEV_TIMEOUT, drains the copies
+// and MMAs already issued, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "attn.cuh"
+#include "tc_ptx.cuh"
+
+namespace ddt {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kKeys = 64;                 // keys per pipeline tile
+constexpr int kStages = 4;
+constexpr int kThreads = 512;
+constexpr int kD = 128;                   // head dim of this path
+constexpr int kMaxSide = 8;               // leftover rows handled on mma.sync
+
+constexpr uint32_t kQTileBytes = 128 * kD * 2;          // 32 KB (two 16 KB halves)
+constexpr uint32_t kHalfBytes = kKeys * 128;            // 8 KB: 64 rows x 128 B
+constexpr uint32_t kStageBytes = 4 * kHalfBytes;        // K0 K1 V0 V1
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffStages = 2 * kQTileBytes;                       // 64 KB
+constexpr uint32_t kOffSideO = kOffStages + kStages * kStageBytes;     // 192 KB
+constexpr uint32_t kSideOBytes = kD * kMaxSide * 4;                    // 4 KB
+constexpr uint32_t kSmemBytes = kOffSideO + kSideOBytes + 1024;        // + alignment slack
+
+constexpr uint32_t kColS = 0;     // + 64 * t
+constexpr uint32_t kColO = 128;   // + 128 * t
+
+struct TcMaps {
+    CUtensorMap q;    // {Dh, G, Hkv, B*N}
+    CUtensorMap kc;   // {Dh, Hkv, page_size, num_pages}
+    CUtensorMap vc;
+    CUtensorMap kt;   // {Dh, Hkv, B*N}
+    CUtensorMap vt;
+};
+
+struct TcShared {
+    uint64_t q_full;
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_final;
+    uint64_t vfix[3];
+    uint32_t tmem_base;
+    int abort;
+    float side_max[2][4][kMaxSide];
+    float side_l[4][kMaxSide];
+    float side_m[kMaxSide];
+};
+
+struct Geometry {
+    int b, kvh, chunk, L, nn, nchunks, t_begin, n_ctx, n_tree, n_tiles;
+    int R, G, n_main, n_side;
+    bool bad;
+};
+
+// key range of pipeline tile j: first key, number of valid keys, and the
+// index of its V fix-up barrier (-1: none)
+struct TileInfo {
+    bool ctx;
+    int key0, valid, fix;
+};
+
+DDT_DEVINL TileInfo tile_info(const Geometry& g, int j) {
+    TileInfo ti;
+    if (j < g.n_ctx) {
+        ti.ctx = true;
+        ti.key0 = (g.t_begin + j) * kKeys;
+        ti.valid = min(kKeys, g.L - ti.key0);
+        ti.fix = ti.valid < kKeys ? 0 : -1;
+    } else {
+        const int tt = j - g.n_ctx;
+        ti.ctx = false;
+        ti.key0 = tt * kKeys;
+        ti.valid = max(0, min(kKeys, g.nn - ti.key0));
+        ti.fix = 1 + tt;
+    }
+    return ti;
+}
+
+DDT_DEVINL uint32_t bar_addr(const uint64_t& b) { return smem_u32(&b); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ TcShared sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    Geometry g;
+    g.b = blockIdx.z;
+    g.kvh = blockIdx.y;
+    g.chunk = blockIdx.x;
+    g.G = p.G;
+    g.R = p.R;
+    g.L = p.ctx_len[g.b];
+    g.bad = false;
+    if (g.L < 0 || g.L > p.max_pages * p.page_size) { g.bad = true; g.L = 0; }
+    const int nt_ctx = (g.L + kKeys - 1) / kKeys;
+    g.nchunks = nt_ctx > 0 ? (nt_ctx + p.tiles_per_chunk - 1) / p.tiles_per_chunk : 1;
+    if (g.chunk >= g.nchunks) return;
+    g.nn = p.n_nodes[g.b];
+    if (g.nn < 0 || g.nn > p.N) { g.bad = true; g.nn = 0; }
+    g.t_begin = g.chunk * p.tiles_per_chunk;
+    g.n_ctx = max(0, min(nt_ctx, g.t_begin + p.tiles_per_chunk) - g.t_begin);
+    g.n_tree = (g.chunk == g.nchunks - 1) ? (p.N + kKeys - 1) / kKeys : 0;
+    g.n_tiles = g.n_ctx + g.n_tree;
+    g.n_main = g.R > 128 ? 2 : 1;
+    g.n_side = max(0, g.R - 256);
+
+    if (g.bad) {   // the request's rows are zeros
+        if (g.chunk == 0) {
+            if (tid == 0) report(p.dev_status, DDT_DEV_BAD_CTX);
+            for (int x = tid; x < g.R * (kD / 8); x += kThreads) {
+                const int r = x / (kD / 8), c = x % (kD / 8);
+                const int i = r / g.G, h = g.kvh * g.G + r % g.G;
+                *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD + c * 8) =
+                    make_uint4(0, 0, 0, 0);
+                if (p.lse && c == 0) p.lse[(static_cast<size_t>(g.b) * p.N + i) * p.Hq + h] = -INFINITY;
+            }
+        }
+        return;
+    }
+
+    const size_t slot = (static_cast<size_t>(g.b) * p.Hkv + g.kvh) * p.max_chunks + g.chunk;
+    const bool split = g.nchunks > 1;
+
+    // ---------------- set-up: barriers and TMEM ----------------
+    if (tid == 0) {
+        mbar_init(bar_addr(sh.q_full), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_addr(sh.kv_full[s]), 1);
+            mbar_init(bar_addr(sh.kv_empty[s]), g.n_side > 0 ? 2 : 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar_addr(sh.s_full[t]), 1);
+            mbar_init(bar_addr(sh.p_full[t]), 128);
+        }
+        mbar_init(bar_addr(sh.o_final), 1);
+        for (int k = 0; k < 3; ++k) mbar_init(bar_addr(sh.vfix[k]), 1);
+        sh.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&sh.tmem_base), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sh.tmem_base;
+    volatile int* abort = &sh.abort;
+
+    const uint32_t sQ = smem_u32(smem + kOffQ);
+    const uint32_t sStage = smem_u32(smem + kOffStages);
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        const int box_keys = p.page_size < kKeys ? p.page_size : kKeys;
+        int last_issued[kStages];
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
+        if (lane == 0) {
+            prefetch_tmap(&maps.q);
+            prefetch_tmap(&maps.kc);
+            prefetch_tmap(&maps.vc);
+            prefetch_tmap(&maps.kt);
+            prefetch_tmap(&maps.vt);
+            mbar_arrive_expect_tx(bar_addr(sh.q_full), g.n_main * kQTileBytes);
+            const int nodes_per_tile = 128 / g.G;
+            for (int t = 0; t < g.n_main; ++t)
+                for (int h = 0; h < 2; ++h)
+                    tma_load_4d(sQ + t * kQTileBytes + h * (kQTileBytes / 2), &maps.q,
+                                bar_addr(sh.q_full), 64 * h, 0, g.kvh,
+                                g.b * p.N + t * nodes_per_tile);
+        }
+        for (int j = 0; j < g.n_tiles; ++j) {
+            const int s = j % kStages;
+            if (j >= kStages &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.kv_empty[s]), ((j / kStages) - 1) & 1, abort)))
+                break;
+            const TileInfo ti = tile_info(g, j);
+            const uint32_t kdst = sStage + s * kStageBytes;
+            const uint32_t vdst = kdst + 2 * kHalfBytes;
+            const uint32_t full = bar_addr(sh.kv_full[s]);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full, kStageBytes);
+                if (ti.ctx) {
+                    for (int sub = 0; sub < kKeys / box_keys; ++sub) {
+                        const int kk = ti.key0 + sub * box_keys;
+                        int page = p.num_pages;   // past the pool: the box reads zeros
+                        if (kk < g.L) {
+                            page = p.page_table[static_cast<size_t>(g.b) * p.max_pages + kk / p.page_size];
+                            if (page < 0 || page >= p.num_pages) {
+                                report(p.dev_status, DDT_DEV_BAD_PAGE);
+                                page = p.num_pages;
+                            }
+                        }
+                        const int slot_in_page = kk % p.page_size;
+                        for (int h = 0; h < 2; ++h) {
+                            tma_load_4d(kdst + h * kHalfBytes + sub * box_keys * 128, &maps.kc, full,
+                                        64 * h, g.kvh, slot_in_page, page);
+                            tma_load_4d(vdst + h * kHalfBytes + sub * box_keys * 128, &maps.vc, full,
+                                        64 * h, g.kvh, slot_in_page, page);
+                        }
+                    }
+                } else {
+                    for (int h = 0; h < 2; ++h) {
+                        tma_load_3d(kdst + h * kHalfBytes, &maps.kt, full, 64 * h, g.kvh,
+                                    g.b * p.N + ti.key0);
+                        tma_load_3d(vdst + h * kHalfBytes, &maps.vt, full, 64 * h, g.kvh,
+                                    g.b * p.N + ti.key0);
+                    }
+                }
+            }
+            last_issued[s] = j;
+            __syncwarp();
+            if (ti.fix >= 0) {
+                // zero V rows [valid, 64) once the tile has landed
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(full, (j / kStages) & 1, abort))) break;
+                const int rows = kKeys - ti.valid;
+                for (int x = lane; x < rows * 16; x += 32) {
+                    const int row = ti.valid + x / 16, part = x % 16;   // 16 x 16 B per row (two halves)
+                    const int h = part / 8, c = part % 8;
+                    unsigned char* dst = smem + kOffStages + s * kStageBytes + 2 * kHalfBytes +
+                                         h * kHalfBytes + row * 128 + c * 16;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_addr(sh.vfix[ti.fix]));
+            }
+        }
+        // drain: every copy issued must land before the CTA can exit
+        if (lane == 0) {
+            for (int s = 0; s < kStages; ++s)
+                if (last_issued[s] >= 0) mbar_drain(bar_addr(sh.kv_full[s]), (last_issued[s] / kStages) & 1);
+            mbar_drain(bar_addr(sh.q_full), 0);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t id_s = idesc_bf16_f32(128, kKeys, 0, 0);
+            const uint32_t id_o = idesc_bf16_f32(128, kD, 0, 1);
+            auto qk = [&](int t, int s) {
+                const uint32_t kb = sStage + s * kStageBytes;
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const uint32_t a = sQ + t * kQTileBytes + (ks / 4) * (kQTileBytes / 2) + (ks % 4) * 32;
+                    const uint32_t bk = kb + (ks / 4) * kHalfBytes + (ks % 4) * 32;
+                    mma_ss(tbase + kColS + 64 * t, smem_desc(a, 16, 1024), smem_desc(bk, 16, 1024), id_s,
+                           ks > 0);
+                }
+            };
+            auto pv = [&](int t, int s, bool acc) {
+                const uint32_t vb = sStage + s * kStageBytes + 2 * kHalfBytes;
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    mma_ts(tbase + kColO + 128 * t, tbase + kColS + 64 * t + 8 * ks,
+                           smem_desc(vb + ks * 2048, kHalfBytes, 1024), id_o, acc || ks > 0);
+            };
+            bool ok = mbar_wait_bounded(bar_addr(sh.q_full), 0, abort) &&
+                      (g.n_tiles == 0 || mbar_wait_bounded(bar_addr(sh.kv_full[0]), 0, abort));
+            if (ok && g.n_tiles > 0) {
+                tc_fence_after();
+                qk(0, 0);
+                mma_commit(bar_addr(sh.s_full[0]));
+                if (g.n_main == 2) {
+                    qk(1, 0);
+                    mma_commit(bar_addr(sh.s_full[1]));
+                }
+            }
+            for (int j = 0; ok && j < g.n_tiles; ++j) {
+                const int s = j % kStages;
+                const int s1 = (j + 1) % kStages;
+                const TileInfo ti = tile_info(g, j);
+                if (ti.fix >= 0 && !mbar_wait_bounded(bar_addr(sh.vfix[ti.fix]), 0, abort)) break;
+                if (!mbar_wait_bounded(bar_addr(sh.p_full[0]), j & 1, abort)) break;
+                tc_fence_after();
+                pv(0, s, j > 0);
+                const bool more = j + 1 < g.n_tiles;
+                if (more) {
+                    if (!mbar_wait_bounded(bar_addr(sh.kv_full[s1]), ((j + 1) / kStages) & 1, abort)) break;
+                    tc_fence_after();
+                    qk(0, s1);
+                    mma_commit(bar_addr(sh.s_full[0]));
+                }
+                if (g.n_main == 2) {
+                    if (!mbar_wait_bounded(bar_addr(sh.p_full[1]), j & 1, abort)) break;
+                    tc_fence_after();
+                    pv(1, s, j > 0);
+                }
+                mma_commit(bar_addr(sh.kv_empty[s]));
+                if (g.n_main == 2 && more) {
+                    qk(1, s1);
+                    mma_commit(bar_addr(sh.s_full[1]));
+                }
+            }
+            mma_commit(bar_addr(sh.o_final));
+            mbar_drain(bar_addr(sh.o_final), 0);   // every MMA done before TMEM is freed
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 12) {
+        // ---------------- softmax: one thread per row of tile t ----------------
+        const int t = (warp - 4) / 4;
+        const int qw = warp & 3;
+        const int row_local = 32 * qw + lane;
+        const int r = 128 * t + row_local;
+        const bool active = t < g.n_main;
+        const bool valid_row = active && r < g.R;
+        const int node = valid_row ? r / g.G : 0;
+        const bool real = valid_row && node < g.nn;
+        uint32_t visw[4] = {0u, 0u, 0u, 0u};
+        if (real)
+            for (int w = 0; w < p.W; ++w) visw[w] = p.vis[(static_cast<size_t>(g.b) * p.N + node) * p.W + w];
+        const uint32_t lane_off = static_cast<uint32_t>(32 * qw) << 16;
+        const uint32_t tS = tbase + lane_off + kColS + 64 * t;
+        const uint32_t tO = tbase + lane_off + kColO + 128 * t;
+        float m_ref = -INFINITY, l_sum = 0.0f;
+        bool ok = active;
+        for (int j = 0; ok && j < g.n_tiles; ++j) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.s_full[t]), j & 1, abort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t raw[2][32];
+            tmem_ld32(tS, raw[0]);
+            tmem_ld32(tS + 32, raw[1]);
+            tmem_wait_ld();
+            const TileInfo ti = tile_info(g, j);
+            // visibility bits of this tile's 64 keys (all set on a context tile)
+            uint32_t vlo = 0xFFFFFFFFu, vhi = 0xFFFFFFFFu;
+            if (!ti.ctx) {
+                vlo = pick4(visw, ti.key0 >> 5);
+                vhi = pick4(visw, (ti.key0 >> 5) + 1);
+            }
+            // masked, scaled scores in place (log2 domain)
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const uint32_t bit = c < 32 ? (vlo >> c) & 1u : (vhi >> (c - 32)) & 1u;
+                const bool vis_ok = c < ti.valid && bit;
+                const float v = vis_ok ? __uint_as_float(raw[c >> 5][c & 31]) * p.scale_log2 : -INFINITY;
+                raw[c >> 5][c & 31] = __float_as_uint(v);
+                mx = fmaxf(mx, v);
+            }
+            if (mx > m_ref + 8.0f) {   // raise the reference: rescale O and l
+                if (j > 0 && m_ref != -INFINITY) {
+                    const float alpha = exp2f(m_ref - mx);
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(tO + 32 * c, o);
+                    }
+                    l_sum *= alpha;
+                }
+                m_ref = mx;
+            }
+            const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
+            // P = exp2(s - m) as bf16 pairs, written over the first 32 columns of S
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = exp2f(__uint_as_float(raw[(2 * c) >> 5][(2 * c) & 31]) - m_use);
+                const float p1 = exp2f(__uint_as_float(raw[(2 * c + 1) >> 5][(2 * c + 1) & 31]) - m_use);
+                l_sum += p0 + p1;
+                __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+                raw[0][c] = *reinterpret_cast<uint32_t*>(&v);
+            }
+            tmem_st32(tS, raw[0]);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar_addr(sh.p_full[t]));
+        }
+        if (active) {
+            const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.o_final), 0, abort));
+            tc_fence_after();
+            const int i = node, h = g.kvh * g.G + (valid_row ? r % g.G : 0);
+            const bool good = done && ok;
+            if (!split) {
+                const float inv = (real && good && l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
+                bf16_t* dst = p.out + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_wait_ld();
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
+                                                                 __uint_as_float(o[2 * e + 1]) * inv);
+                        w[e] = *reinterpret_cast<uint32_t*>(&v);
+                    }
+                    if (valid_row) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) =
+                                make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    }
+                }
+                if (p.lse && valid_row)
+                    p.lse[(static_cast<size_t>(g.b) * p.N + i) * p.Hq + h] =
+                        (real && good && l_sum > 0.0f) ? (m_ref + log2f(l_sum)) * 0.69314718055994531f
+                                                       : -INFINITY;
+            } else {
+                float* dst = p.ws_o + (slot * p.R + (valid_row ? r : 0)) * kD;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_wait_ld();
+                    if (valid_row) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            *reinterpret_cast<float4*>(dst + 32 * c + 4 * e) =
+                                make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                            __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    }
+                }
+                if (valid_row)
+                    p.ws_ml[slot * p.R + r] = good ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.0f);
+            }
+        }
+    } else if (warp >= 12 && g.n_side > 0) {
+        // ---------------- leftover rows on mma.sync ----------------
+        const int sw = warp - 12;                      // keys 16*sw .. 16*sw+15 of each tile
+        const int nrow = lane >> 2;                    // B-fragment row (n index)
+        const int crow0 = 2 * (lane & 3);              // C-fragment rows crow0, crow0+1
+        // Q rows as B fragments (k = dh, n = row)
+        uint32_t qb[kD / 16][2];
+        {
+            const int sr = nrow;
+            const bool ok = sr < g.n_side;
+            const int r = 256 + (ok ? sr : 0);
+            const int i = r / g.G, h = g.kvh * g.G + r % g.G;
+            const bf16_t* qrow = p.q + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD;
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const int k0 = ks * 16 + 2 * (lane & 3);
+                qb[ks][0] = ok ? *reinterpret_cast<const uint32_t*>(qrow + k0) : 0u;
+                qb[ks][1] = ok ? *reinterpret_cast<const uint32_t*>(qrow + k0 + 8) : 0u;
+            }
+        }
+        int node_r[2];
+        uint32_t visr[2][4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int sr = crow0 + q;
+            node_r[q] = sr < g.n_side ? (256 + sr) / g.G : -1;
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                visr[q][w] = (node_r[q] >= 0 && node_r[q] < g.nn && w < p.W)
+                                 ? p.vis[(static_cast<size_t>(g.b) * p.N + node_r[q]) * p.W + w] : 0u;
+        }
+        float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.0f, 0.0f};
+        float oacc[kD / 16][4];
+#pragma unroll
+        for (int mb = 0; mb < kD / 16; ++mb) oacc[mb][0] = oacc[mb][1] = oacc[mb][2] = oacc[mb][3] = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < g.n_tiles; ++j) {
+            const int s = j % kStages;
+            const TileInfo ti = tile_info(g, j);
+            bool got = mbar_wait_bounded(bar_addr(sh.kv_full[s]), (j / kStages) & 1, abort);
+            if (got && ti.fix >= 0) got = mbar_wait_bounded(bar_addr(sh.vfix[ti.fix]), 0, abort);
+            if (!__all_sync(0xffffffffu, got)) ok = false;
+            const unsigned char* kst = smem + kOffStages + s * kStageBytes;
+            const unsigned char* vst = kst + 2 * kHalfBytes;
+            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (ok) {
+#pragma unroll
+                for (int ks = 0; ks < kD / 16; ++ks) {
+                    const int key = 16 * sw + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int chunk = ks * 2 + (lane >> 4);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(smem_u32(kst + (chunk >> 3) * kHalfBytes + sw128_offset(key, chunk & 7)),
+                            a0, a1, a2, a3);
+                    mma16816(c, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
+            }
+            // scale, mask; c0/c1: key kA rows crow0/crow0+1; c2/c3: key kA+8
+            const int kA = 16 * sw + nrow;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kl = kA + ((e >> 1) << 3);
+                const int q = e & 1;
+                bool vis_ok = node_r[q] >= 0 && kl < ti.valid;
+                if (!ti.ctx && vis_ok) {
+                    const int key = ti.key0 + kl;
+                    vis_ok = (pick4(visr[q], key >> 5) >> (key & 31)) & 1u;
+                }
+                c[e] = (ok && vis_ok) ? c[e] * p.scale_log2 : -INFINITY;
+            }
+            float mx[2] = {fmaxf(c[0], c[2]), fmaxf(c[1], c[3])};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 4));
+                mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 8));
+                mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 16));
+            }
+            if (lane < 4) {
+                sh.side_max[j & 1][sw][crow0] = mx[0];
+                sh.side_max[j & 1][sw][crow0 + 1] = mx[1];
+            }
+            named_bar_sync(1, 128);
+            float alpha[2], m_use[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float tm = sh.side_max[j & 1][0][crow0 + q];
+#pragma unroll
+                for (int w = 1; w < 4; ++w) tm = fmaxf(tm, sh.side_max[j & 1][w][crow0 + q]);
+                const float m_new = fmaxf(m_run[q], tm);
+                m_use[q] = (m_new == -INFINITY) ? 0.0f : m_new;
+                alpha[q] = exp2f(m_run[q] - m_use[q]);
+                m_run[q] = m_new;
+            }
+            float pe[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pe[e] = exp2f(c[e] - m_use[e & 1]);
+            l_part[0] = l_part[0] * alpha[0] + pe[0] + pe[2];
+            l_part[1] = l_part[1] * alpha[1] + pe[1] + pe[3];
+#pragma unroll
+            for (int mb = 0; mb < kD / 16; ++mb) {
+                oacc[mb][0] *= alpha[0]; oacc[mb][2] *= alpha[0];
+                oacc[mb][1] *= alpha[1]; oacc[mb][3] *= alpha[1];
+            }
+            __nv_bfloat162 p01 = __floats2bfloat162_rn(pe[0], pe[1]);
+            __nv_bfloat162 p23 = __floats2bfloat162_rn(pe[2], pe[3]);
+            const uint32_t b0 = movmatrix_t(*reinterpret_cast<uint32_t*>(&p01));
+            const uint32_t b1 = movmatrix_t(*reinterpret_cast<uint32_t*>(&p23));
+            if (ok) {
+#pragma unroll
+                for (int mb = 0; mb < kD / 16; ++mb) {
+                    const int key = 16 * sw + (lane & 7) + (lane >> 4) * 8;
+                    const int chunk = mb * 2 + ((lane >> 3) & 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_t(smem_u32(vst + (chunk >> 3) * kHalfBytes + sw128_offset(key, chunk & 7)),
+                              a0, a1, a2, a3);
+                    mma16816(oacc[mb], a0, a1, a2, a3, b0, b1);
+                }
+            }
+            named_bar_sync(1, 128);
+            if (sw == 0 && lane == 0 && ok) mbar_arrive(bar_addr(sh.kv_empty[s]));
+        }
+        // combine the four warps' partial sums (each covers its 16 keys of every tile)
+        float* side_o = reinterpret_cast<float*>(smem + kOffSideO);   // [kD][kMaxSide]
+        for (int x = tid - 384; x < kD * kMaxSide; x += 128) side_o[x] = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            l_part[q] += __shfl_xor_sync(0xffffffffu, l_part[q], 4);
+            l_part[q] += __shfl_xor_sync(0xffffffffu, l_part[q], 8);
+            l_part[q] += __shfl_xor_sync(0xffffffffu, l_part[q], 16);
+        }
+        if (lane < 4) {
+            sh.side_l[sw][crow0] = l_part[0];
+            sh.side_l[sw][crow0 + 1] = l_part[1];
+            if (sw == 0) {
+                sh.side_m[crow0] = m_run[0];
+                sh.side_m[crow0 + 1] = m_run[1];
+            }
+        }
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int mb = 0; mb < kD / 16; ++mb) {
+            const int d0 = 16 * mb + nrow;
+            atomicAdd(&side_o[d0 * kMaxSide + crow0], oacc[mb][0]);
+            atomicAdd(&side_o[d0 * kMaxSide + crow0 + 1], oacc[mb][1]);
+            atomicAdd(&side_o[(d0 + 8) * kMaxSide + crow0], oacc[mb][2]);
+            atomicAdd(&side_o[(d0 + 8) * kMaxSide + crow0 + 1], oacc[mb][3]);
+        }
+        named_bar_sync(1, 128);
+        // write: thread -> (row tid/16, 8 features)
+        const int st = tid - 384;
+        const int sr = st >> 4, d0 = (st & 15) * 8;
+        if (sr < g.n_side) {
+            const int r = 256 + sr;
+            const int i = r / g.G, h = g.kvh * g.G + r % g.G;
+            const float lt = sh.side_l[0][sr] + sh.side_l[1][sr] + sh.side_l[2][sr] + sh.side_l[3][sr];
+            const float mrun = sh.side_m[sr];   // the same in every side warp
+            const bool real = i < g.nn && ok;
+            if (!split) {
+                const float inv = (real && lt > 0.0f) ? 1.0f / lt : 0.0f;
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    __nv_bfloat162 v = __floats2bfloat162_rn(side_o[(d0 + 2 * e) * kMaxSide + sr] * inv,
+                                                             side_o[(d0 + 2 * e + 1) * kMaxSide + sr] * inv);
+                    w[e] = *reinterpret_cast<uint32_t*>(&v);
+                }
+                *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD + d0) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+                if (p.lse && d0 == 0)
+                    p.lse[(static_cast<size_t>(g.b) * p.N + i) * p.Hq + h] =
+                        (real && lt > 0.0f) ? (mrun + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+            } else {
+                float* dst = p.ws_o + (slot * p.R + r) * kD + d0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dst[e] = side_o[(d0 + e) * kMaxSide + sr];
+                if (d0 == 0) p.ws_ml[slot * p.R + r] = ok ? make_float2(mrun, lt) : make_float2(-INFINITY, 0.0f);
+            }
+        }
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tbase, 512);
+    if (tid == 0 && sh.abort) report(p.dev_status, DDT_DEV_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// host: tensor maps and launch
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool encode(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* base, int rank,
+            const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                    strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// True when tree_verify_attn's sizes fit the tensor-core kernel.
+bool attn_tc_supported(const AttnParams& p) {
+    if (p.Dh != kD || 128 % p.G != 0) return false;
+    if (p.R > 256 + kMaxSide || p.n_groups != 1) return false;
+    if (p.page_size < kKeys ? (kKeys % p.page_size) != 0 : (p.page_size % kKeys) != 0) return false;
+    return true;
+}
+
+cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t stream) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = get_encode();
+    if (!fn) return cudaErrorNotSupported;
+    TcMaps maps;
+    const cuuint64_t es = 2;
+    {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.G),
+                                    static_cast<cuuint64_t>(p.Hkv), static_cast<cuuint64_t>(p.B) * p.N};
+        const cuuint64_t str[3] = {kD * es, static_cast<cuuint64_t>(p.G) * kD * es,
+                                   static_cast<cuuint64_t>(p.Hq) * kD * es};
+        const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(p.G), 1, static_cast<cuuint32_t>(128 / p.G)};
+        if (!encode(fn, &maps.q, p.q, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.Hkv),
+                                    static_cast<cuuint64_t>(p.page_size), static_cast<cuuint64_t>(p.num_pages)};
+        const cuuint64_t str[3] = {kD * es, static_cast<cuuint64_t>(p.Hkv) * kD * es,
+                                   static_cast<cuuint64_t>(p.page_size) * p.Hkv * kD * es};
+        const cuuint32_t bk = static_cast<cuuint32_t>(p.page_size < kKeys ? p.page_size : kKeys);
+        const cuuint32_t box[4] = {64, 1, bk, 1};
+        if (!encode(fn, &maps.kc, p.k_cache, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode(fn, &maps.vc, p.v_cache, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(p.Hkv),
+                                    static_cast<cuuint64_t>(p.B) * p.N};
+        const cuuint64_t str[2] = {kD * es, static_cast<cuuint64_t>(p.Hkv) * kD * es};
+        const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kKeys)};
+        if (!encode(fn, &maps.kt, p.k_tree, 3, dims, str, box)) return cudaErrorInvalidValue;
+        if (!encode(fn, &maps.vt, p.v_tree, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    const dim3 grid(p.max_chunks, p.Hkv, p.B);
+    attn_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, maps);
+    return cudaGetLastError();
+}
+
+}  // namespace ddt

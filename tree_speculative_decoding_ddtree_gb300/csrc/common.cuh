@@ -55,4 +55,9 @@ DDT_DEVINL float warp_sum_f(float v) {
     return v;
 }
 
+// v[i] for a runtime i in 0..3 without indexing a register array (selects only)
+DDT_DEVINL uint32_t pick4(const uint32_t (&v)[4], int i) {
+    return i == 0 ? v[0] : (i == 1 ? v[1] : (i == 2 ? v[2] : v[3]));
+}
+
 }  // namespace ddt
