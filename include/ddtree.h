@@ -61,7 +61,9 @@ enum ddtree_status {
     DDT_ESHAPE = -2,      /* sizes outside the supported range                */
     DDT_ECUDA = -3,       /* a CUDA runtime call or launch failed             */
     DDT_ETIMEOUT = -4,    /* reserved: a bounded device wait gave up          */
-    DDT_EWORKSPACE = -6   /* workspace pointer null or smaller than required  */
+    DDT_EWORKSPACE = -6,  /* workspace pointer null or smaller than required  */
+    DDT_ESCRATCH = -7     /* sizes need more scratch than the fixed array of  */
+                          /* tree_verify_attn_noalloc holds                   */
 };
 
 /* bits OR-ed into *dev_status by the device */
@@ -248,6 +250,40 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                          uint64_t philox_offset, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
                          int32_t* dev_status, void* stream);
+
+/*
+ * tree_verify_attn_noalloc - tree_verify_attn without a caller workspace.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory at run time (for example a serving engine
+ * that reserves nearly all of HBM for its own KV pool at start-up and gives
+ * plugins no allocator, or a hot loop where a cudaMalloc would stall the
+ * device). Arguments, outputs and results are those of tree_verify_attn
+ * minus the workspace. The split-KV scratch comes from one fixed device array
+ * inside the library, of tree_verify_attn_noalloc_max_scratch() bytes
+ * (64 MiB), which every GPU that loads the library holds until the process
+ * exits. The call allocates nothing and frees nothing.
+ *
+ * - Sizes whose scratch need (tree_verify_attn_workspace_size) exceeds the
+ *   array are rejected with DDT_ESCRATCH before anything is launched.
+ * - The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ * - All calls share the array and it keeps the last call's contents; every
+ *   scratch word a call reads is written earlier in the same call, so nothing
+ *   is cleared. Calls that overlap on the GPU (unordered streams, or several
+ *   host threads) race on the array and must be serialised by the caller.
+ */
+int tree_verify_attn_noalloc(const ddtree_bf16* q, const ddtree_bf16* k_tree,
+                             const ddtree_bf16* v_tree, const ddtree_bf16* k_cache,
+                             const ddtree_bf16* v_cache, int num_pages, int page_size,
+                             const int32_t* page_table, int max_pages,
+                             const int32_t* ctx_len, const uint32_t* vis,
+                             const int32_t* n_nodes, int B, int N, int Hq, int Hkv,
+                             int Dh, float scale, ddtree_bf16* out, float* lse,
+                             int32_t* dev_status, void* stream);
+
+/* Size in bytes of the fixed scratch array behind tree_verify_attn_noalloc. */
+size_t tree_verify_attn_noalloc_max_scratch(void);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,7 @@ from . import _build
 __all__ = [
     "DDTreeError", "load_library", "library_path", "ddtree_build", "tree_verify_attn",
     "tree_verify_attn_workspace_size", "ddtree_accept_greedy", "ddtree_accept_sample",
-    "TreeBuffers", "alloc_tree", "DEV_ERRORS",
+    "TreeBuffers", "alloc_tree", "DEV_ERRORS", "tree_verify_attn_noalloc",
 ]
 
 DEV_ERRORS = {
@@ -252,3 +252,40 @@ def ddtree_accept_sample(logits: torch.Tensor, tree: TreeBuffers, D: int,
         _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
     _check(st, "ddtree_accept_sample")
     return o
+
+
+def tree_verify_attn_noalloc(q: torch.Tensor, k_tree: torch.Tensor, v_tree: torch.Tensor,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             page_table: torch.Tensor, ctx_len: torch.Tensor, vis: torch.Tensor,
+                             n_nodes: torch.Tensor, scale: float, out: torch.Tensor,
+                             lse: Optional[torch.Tensor] = None,
+                             dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Tree-verify attention through ``tree_verify_attn_noalloc``: for callers that
+    cannot allocate device memory at run time. The split-KV scratch is the library's
+    own fixed 64 MiB device array (shared by all calls; calls that overlap on the GPU
+    race on it), and ``out`` must be given, so this call allocates nothing."""
+    lib = load_library()
+    fn = lib.tree_verify_attn_noalloc
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P, I, I, I, I, I, F, P, P, P, P]
+    B, N, Hq, Dh = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    max_pages = page_table.shape[1]
+    W = (N + 31) // 32
+    st = fn(_ptr(q, torch.bfloat16, "q", (B, N, Hq, Dh)),
+            _ptr(k_tree, torch.bfloat16, "k_tree", (B, N, Hkv, Dh)),
+            _ptr(v_tree, torch.bfloat16, "v_tree", (B, N, Hkv, Dh)),
+            _ptr(k_cache, torch.bfloat16, "k_cache", (num_pages, page_size, Hkv, Dh)),
+            _ptr(v_cache, torch.bfloat16, "v_cache", (num_pages, page_size, Hkv, Dh)),
+            num_pages, page_size,
+            _ptr(page_table, torch.int32, "page_table", (B, max_pages)), max_pages,
+            _ptr(ctx_len, torch.int32, "ctx_len", (B,)),
+            _ptr(vis, torch.int32, "vis", (B, N, W)),
+            _ptr(n_nodes, torch.int32, "n_nodes", (B,)),
+            B, N, Hq, Hkv, Dh, float(scale),
+            _ptr(out, torch.bfloat16, "out", (B, N, Hq, Dh)),
+            _ptr(lse, torch.float32, "lse", (B, N, Hq)),
+            _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
+    _check(st, "tree_verify_attn_noalloc")
+    return out

@@ -66,6 +66,12 @@ bool plan_attn(int B, int N, int Hq, int Hkv, int Dh, long long max_ctx, AttnPla
 
 }  // namespace
 
+// Record a CUDA failure for ddtree_last_error() (used by entry points in other files).
+void set_last_error(const char* what, cudaError_t e) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s: %s", what, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+}
+
 }  // namespace ddt
 
 using namespace ddt;
@@ -80,6 +86,7 @@ const char* ddtree_status_string(int status) {
         case DDT_ECUDA: return "DDT_ECUDA: a CUDA call or launch failed";
         case DDT_ETIMEOUT: return "DDT_ETIMEOUT: a bounded device wait gave up";
         case DDT_EWORKSPACE: return "DDT_EWORKSPACE: workspace missing or too small";
+        case DDT_ESCRATCH: return "DDT_ESCRATCH: sizes need more scratch than tree_verify_attn_noalloc's fixed array";
         default: return "unknown ddtree status";
     }
 }
