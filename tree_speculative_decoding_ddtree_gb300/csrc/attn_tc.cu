@@ -27,7 +27,9 @@
 //   warps 12-15  the leftover rows on mma.sync (keys on M, rows on N), reading
 //                the same K/V stages through ldmatrix.
 //
-// TMEM columns: S0/P0 [0,64), S1/P1 [64,128), O0 [128,256), O1 [256,384).
+// TMEM columns: S/P of tile t, buffer u at [64*(2t+u), +64); O_t at [256+128t, +128).
+// With two S buffers per tile the tensor core computes S for key tile j+1
+// while the softmax of key tile j runs.
 // Every wait is bounded; a timeout sets DDT_DEV_TIMEOUT, drains the copies
 // and MMAs already issued, frees TMEM and returns.
 #include <cuda.h>
@@ -57,8 +59,8 @@ constexpr uint32_t kOffSideO = kOffStages + kStages * kStageBytes;     // 192 KB
 constexpr uint32_t kSideOBytes = kD * kMaxSide * 4;                    // 4 KB
 constexpr uint32_t kSmemBytes = kOffSideO + kSideOBytes + 1024;        // + alignment slack
 
-constexpr uint32_t kColS = 0;     // + 64 * t
-constexpr uint32_t kColO = 128;   // + 128 * t
+constexpr uint32_t kColS = 0;     // + 64 * (2 * t + buf): two S/P buffers per tile
+constexpr uint32_t kColO = 256;   // + 128 * t
 
 struct TcMaps {
     CUtensorMap q;    // {Dh, G, Hkv, B*N}
@@ -72,8 +74,9 @@ struct TcShared {
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t s_full[2][2];    // [tile][buffer]: S of a key tile is in TMEM
+    uint64_t p_full[2][2];    // [tile][buffer]: P written over it
+    uint64_t o_done[2];       // PV of a key tile finished accumulating into O
     uint64_t o_final;
     uint64_t vfix[3];
     uint32_t tmem_base;
@@ -170,8 +173,11 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             mbar_init(bar_addr(sh.kv_empty[s]), g.n_side > 0 ? 2 : 1);
         }
         for (int t = 0; t < 2; ++t) {
-            mbar_init(bar_addr(sh.s_full[t]), 1);
-            mbar_init(bar_addr(sh.p_full[t]), 128);
+            for (int u = 0; u < 2; ++u) {
+                mbar_init(bar_addr(sh.s_full[t][u]), 1);
+                mbar_init(bar_addr(sh.p_full[t][u]), 128);
+            }
+            mbar_init(bar_addr(sh.o_done[t]), 1);
         }
         mbar_init(bar_addr(sh.o_final), 1);
         for (int k = 0; k < 3; ++k) mbar_init(bar_addr(sh.vfix[k]), 1);
@@ -276,58 +282,55 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16_f32(128, kKeys, 0, 0);
             const uint32_t id_o = idesc_bf16_f32(128, kD, 0, 1);
-            auto qk = [&](int t, int s) {
-                const uint32_t kb = sStage + s * kStageBytes;
+            // S_t[j % 2] = Q_t K_j^T
+            auto qk = [&](int t, int j) {
+                const uint32_t kb = sStage + (j % kStages) * kStageBytes;
+                const uint32_t d = tbase + kColS + 64 * (2 * t + (j & 1));
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
                     const uint32_t a = sQ + t * kQTileBytes + (ks / 4) * (kQTileBytes / 2) + (ks % 4) * 32;
                     const uint32_t bk = kb + (ks / 4) * kHalfBytes + (ks % 4) * 32;
-                    mma_ss(tbase + kColS + 64 * t, smem_desc(a, 16, 1024), smem_desc(bk, 16, 1024), id_s,
-                           ks > 0);
+                    mma_ss(d, smem_desc(a, 16, 1024), smem_desc(bk, 16, 1024), id_s, ks > 0);
                 }
+                mma_commit(bar_addr(sh.s_full[t][j & 1]));
             };
-            auto pv = [&](int t, int s, bool acc) {
-                const uint32_t vb = sStage + s * kStageBytes + 2 * kHalfBytes;
+            // O_t (+)= P_t[j % 2] V_j
+            auto pv = [&](int t, int j) {
+                const uint32_t vb = sStage + (j % kStages) * kStageBytes + 2 * kHalfBytes;
+                const uint32_t a = tbase + kColS + 64 * (2 * t + (j & 1));
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tbase + kColO + 128 * t, tbase + kColS + 64 * t + 8 * ks,
-                           smem_desc(vb + ks * 2048, kHalfBytes, 1024), id_o, acc || ks > 0);
+                    mma_ts(tbase + kColO + 128 * t, a + 8 * ks, smem_desc(vb + ks * 2048, kHalfBytes, 1024),
+                           id_o, (j > 0) || ks > 0);
+                mma_commit(bar_addr(sh.o_done[t]));
             };
-            bool ok = mbar_wait_bounded(bar_addr(sh.q_full), 0, abort) &&
-                      (g.n_tiles == 0 || mbar_wait_bounded(bar_addr(sh.kv_full[0]), 0, abort));
-            if (ok && g.n_tiles > 0) {
+            auto k_ready = [&](int j) {
+                return mbar_wait_bounded(bar_addr(sh.kv_full[j % kStages]), (j / kStages) & 1, abort);
+            };
+            bool ok = mbar_wait_bounded(bar_addr(sh.q_full), 0, abort);
+            // prologue: S for key tiles 0 and 1
+            for (int j = 0; ok && j < 2 && j < g.n_tiles; ++j) {
+                if (!k_ready(j)) { ok = false; break; }
                 tc_fence_after();
-                qk(0, 0);
-                mma_commit(bar_addr(sh.s_full[0]));
-                if (g.n_main == 2) {
-                    qk(1, 0);
-                    mma_commit(bar_addr(sh.s_full[1]));
-                }
+                qk(0, j);
+                if (g.n_main == 2) qk(1, j);
             }
             for (int j = 0; ok && j < g.n_tiles; ++j) {
-                const int s = j % kStages;
-                const int s1 = (j + 1) % kStages;
                 const TileInfo ti = tile_info(g, j);
                 if (ti.fix >= 0 && !mbar_wait_bounded(bar_addr(sh.vfix[ti.fix]), 0, abort)) break;
-                if (!mbar_wait_bounded(bar_addr(sh.p_full[0]), j & 1, abort)) break;
-                tc_fence_after();
-                pv(0, s, j > 0);
-                const bool more = j + 1 < g.n_tiles;
-                if (more) {
-                    if (!mbar_wait_bounded(bar_addr(sh.kv_full[s1]), ((j + 1) / kStages) & 1, abort)) break;
+                bool go = true;
+                for (int t = 0; t < g.n_main; ++t) {
+                    if (!mbar_wait_bounded(bar_addr(sh.p_full[t][j & 1]), (j >> 1) & 1, abort)) { go = false; break; }
                     tc_fence_after();
-                    qk(0, s1);
-                    mma_commit(bar_addr(sh.s_full[0]));
+                    pv(t, j);
                 }
-                if (g.n_main == 2) {
-                    if (!mbar_wait_bounded(bar_addr(sh.p_full[1]), j & 1, abort)) break;
+                if (!go) break;
+                mma_commit(bar_addr(sh.kv_empty[j % kStages]));   // K_j and V_j consumed
+                if (j + 2 < g.n_tiles) {
+                    if (!k_ready(j + 2)) break;
                     tc_fence_after();
-                    pv(1, s, j > 0);
-                }
-                mma_commit(bar_addr(sh.kv_empty[s]));
-                if (g.n_main == 2 && more) {
-                    qk(1, s1);
-                    mma_commit(bar_addr(sh.s_full[1]));
+                    qk(0, j + 2);
+                    if (g.n_main == 2) qk(1, j + 2);
                 }
             }
             mma_commit(bar_addr(sh.o_final));
@@ -348,40 +351,64 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         if (real)
             for (int w = 0; w < p.W; ++w) visw[w] = p.vis[(static_cast<size_t>(g.b) * p.N + node) * p.W + w];
         const uint32_t lane_off = static_cast<uint32_t>(32 * qw) << 16;
-        const uint32_t tS = tbase + lane_off + kColS + 64 * t;
+        const uint32_t tS0 = tbase + lane_off + kColS + 64 * (2 * t);
         const uint32_t tO = tbase + lane_off + kColO + 128 * t;
-        float m_ref = -INFINITY, l_sum = 0.0f;
+        const float sc = p.scale_log2;            // > 0 on this path
+        float m_ref = -INFINITY;                  // reference max, scaled log2 units
+        float l_sum = 0.0f;
         bool ok = active;
         for (int j = 0; ok && j < g.n_tiles; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.s_full[t]), j & 1, abort))) {
+            const int u = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.s_full[t][u]), (j >> 1) & 1, abort))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const uint32_t tS = tS0 + 64 * u;
             uint32_t raw[2][32];
             tmem_ld32(tS, raw[0]);
             tmem_ld32(tS + 32, raw[1]);
             tmem_wait_ld();
             const TileInfo ti = tile_info(g, j);
-            // visibility bits of this tile's 64 keys (all set on a context tile)
-            uint32_t vlo = 0xFFFFFFFFu, vhi = 0xFFFFFFFFu;
-            if (!ti.ctx) {
-                vlo = pick4(visw, ti.key0 >> 5);
-                vhi = pick4(visw, (ti.key0 >> 5) + 1);
-            }
-            // masked, scaled scores in place (log2 domain)
-            float mx = -INFINITY;
+            if (!(ti.ctx && ti.valid == kKeys)) {
+                // ragged context tail or tree tile: masked scores become -inf
+                uint32_t vlo = 0xFFFFFFFFu, vhi = 0xFFFFFFFFu;
+                if (!ti.ctx) {
+                    vlo = pick4(visw, ti.key0 >> 5);
+                    vhi = pick4(visw, (ti.key0 >> 5) + 1);
+                }
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const uint32_t bit = c < 32 ? (vlo >> c) & 1u : (vhi >> (c - 32)) & 1u;
-                const bool vis_ok = c < ti.valid && bit;
-                const float v = vis_ok ? __uint_as_float(raw[c >> 5][c & 31]) * p.scale_log2 : -INFINITY;
-                raw[c >> 5][c & 31] = __float_as_uint(v);
-                mx = fmaxf(mx, v);
+                for (int c = 0; c < 64; ++c) {
+                    const uint32_t bit = c < 32 ? (vlo >> c) & 1u : (vhi >> (c - 32)) & 1u;
+                    if (!(c < ti.valid && bit)) raw[c >> 5][c & 31] = 0xFF800000u;   // -inf
+                }
             }
-            if (mx > m_ref + 8.0f) {   // raise the reference: rescale O and l
+            // row max of the raw scores (scale > 0 keeps the order), as a tree
+            float mx;
+            {
+                float m8[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int c0 = 8 * q;
+                    const float a0 = fmaxf(__uint_as_float(raw[c0 >> 5][c0 & 31]), __uint_as_float(raw[(c0 + 1) >> 5][(c0 + 1) & 31]));
+                    const float a1 = fmaxf(__uint_as_float(raw[(c0 + 2) >> 5][(c0 + 2) & 31]), __uint_as_float(raw[(c0 + 3) >> 5][(c0 + 3) & 31]));
+                    const float a2 = fmaxf(__uint_as_float(raw[(c0 + 4) >> 5][(c0 + 4) & 31]), __uint_as_float(raw[(c0 + 5) >> 5][(c0 + 5) & 31]));
+                    const float a3 = fmaxf(__uint_as_float(raw[(c0 + 6) >> 5][(c0 + 6) & 31]), __uint_as_float(raw[(c0 + 7) >> 5][(c0 + 7) & 31]));
+                    m8[q] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+                }
+                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            }
+            const float mxs = mx * sc;
+            if (mxs > m_ref + 8.0f) {   // raise the reference: rescale O and l
                 if (j > 0 && m_ref != -INFINITY) {
-                    const float alpha = exp2f(m_ref - mx);
+                    // O must hold every earlier key tile before it is rescaled
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_bounded(bar_addr(sh.o_done[t]), (j - 1) & 1, abort))) {
+                        ok = false;
+                    }
+                    tc_fence_after();
+                    const float alpha = fast_exp2(m_ref - mxs);
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
@@ -393,22 +420,24 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                     }
                     l_sum *= alpha;
                 }
-                m_ref = mx;
+                m_ref = mxs;
             }
-            const float m_use = (m_ref == -INFINITY) ? 0.0f : m_ref;
-            // P = exp2(s - m) as bf16 pairs, written over the first 32 columns of S
+            const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+            // P = 2^(s*scale - m) as bf16 pairs over the first 32 columns of this S buffer
+            float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float p0 = exp2f(__uint_as_float(raw[(2 * c) >> 5][(2 * c) & 31]) - m_use);
-                const float p1 = exp2f(__uint_as_float(raw[(2 * c + 1) >> 5][(2 * c + 1) & 31]) - m_use);
-                l_sum += p0 + p1;
+                const float p0 = fast_exp2(fmaf(__uint_as_float(raw[(2 * c) >> 5][(2 * c) & 31]), sc, neg_m));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(raw[(2 * c + 1) >> 5][(2 * c + 1) & 31]), sc, neg_m));
+                ls[c & 3] += p0 + p1;
                 __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
                 raw[0][c] = *reinterpret_cast<uint32_t*>(&v);
             }
+            l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tmem_st32(tS, raw[0]);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_addr(sh.p_full[t]));
+            mbar_arrive(bar_addr(sh.p_full[t][u]));
         }
         if (active) {
             const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.o_final), 0, abort));
@@ -677,7 +706,7 @@ bool encode(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* ba
 
 // True when tree_verify_attn's sizes fit the tensor-core kernel.
 bool attn_tc_supported(const AttnParams& p) {
-    if (p.Dh != kD || 128 % p.G != 0) return false;
+    if (p.Dh != kD || 128 % p.G != 0 || !(p.scale_log2 > 0.0f)) return false;
     if (p.R > 256 + kMaxSide || p.n_groups != 1) return false;
     if (p.page_size < kKeys ? (kKeys % p.page_size) != 0 : (p.page_size % kKeys) != 0) return false;
     return true;

@@ -224,6 +224,13 @@ TC_DEVINL void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;\n" :: "r"(id), "r"(nthreads) : "memory");
 }
 
+// 2^x on the MUFU unit (ex2.approx, flush-to-zero): 2^-inf = +0
+TC_DEVINL float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte-swizzled
 // region whose rows are 128 bytes and whose base is 1024-byte aligned
 TC_DEVINL uint32_t sw128_offset(int row, int chunk) {
