@@ -9,12 +9,13 @@
 // Tree Sampling for DDTree", Path B (lazy softmax of the visited nodes only).
 //
 // One CTA per request walks the tree; only the logits rows of visited nodes
-// are read, each streamed once per pass with 16-byte loads.
+// are read, each streamed once per pass with 16-byte loads, eight in flight
+// per thread so a row costs about one memory round trip.
 #include "common.cuh"
 
 namespace ddt {
 
-constexpr int kAcceptThreads = 512;
+constexpr int kAcceptThreads = 1024;
 constexpr int kMaxKids = DDT_MAX_TOPK;
 
 // ---------------------------------------------------------------------------
@@ -76,6 +77,7 @@ DDT_DEVINL uint32_t row_argmax(const float* __restrict__ row, int V, bool vec4,
     unsigned long long best = 0ull;
     if (vec4) {
         const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 8
         for (int x = threadIdx.x; x < (V >> 2); x += kAcceptThreads) {
             const float4 f = __ldg(r4 + x);
             const uint32_t v = static_cast<uint32_t>(x) << 2;
@@ -201,6 +203,7 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         float m = -INFINITY;
         if (vec4) {
             const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 8
             for (int x = threadIdx.x; x < (V >> 2); x += kAcceptThreads) {
                 const float4 f = __ldg(r4 + x);
                 m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
@@ -212,6 +215,7 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         float z = 0.0f;
         if (vec4) {
             const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 8
             for (int x = threadIdx.x; x < (V >> 2); x += kAcceptThreads) {
                 const float4 f = __ldg(r4 + x);
                 z += expf((f.x - m) * inv_t) + expf((f.y - m) * inv_t) +
@@ -265,6 +269,7 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         const int nk = s_nkids;
         unsigned long long best = 0ull;
         const int groups = (V + 3) >> 2;
+#pragma unroll 4
         for (int x = threadIdx.x; x < groups; x += kAcceptThreads) {
             const uint4 w = philox4x32_10(make_uint4(1u | off_hi8, static_cast<uint32_t>(u),
                                                      static_cast<uint32_t>(x), off_lo), k0, k1);

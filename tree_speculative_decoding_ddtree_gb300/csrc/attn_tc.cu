@@ -27,9 +27,10 @@
 //   warps 12-15  the leftover rows on mma.sync (keys on M, rows on N), reading
 //                the same K/V stages through ldmatrix.
 //
-// TMEM columns: S/P of tile t, buffer u at [64*(2t+u), +64); O_t at [256+128t, +128).
-// With two S buffers per tile the tensor core computes S for key tile j+1
-// while the softmax of key tile j runs.
+// TMEM columns: S/P of tile t at [64t, +64); Q of tile t at [128+64t, +64) (the A
+// operand of QK^T, so Q is not re-read from shared memory for every key tile);
+// O of tile t at [256+128t, +128). The tensor core works on one tile while the
+// other tile's softmax runs.
 // Every wait is bounded; a timeout sets DDT_DEV_TIMEOUT, drains the copies
 // and MMAs already issued, frees TMEM and returns.
 #include <cuda.h>
@@ -59,7 +60,8 @@ constexpr uint32_t kOffSideO = kOffStages + kStages * kStageBytes;     // 192 KB
 constexpr uint32_t kSideOBytes = kD * kMaxSide * 4;                    // 4 KB
 constexpr uint32_t kSmemBytes = kOffSideO + kSideOBytes + 1024;        // + alignment slack
 
-constexpr uint32_t kColS = 0;     // + 64 * (2 * t + buf): two S/P buffers per tile
+constexpr uint32_t kColS = 0;     // + 64 * t: S of tile t, P written over its first 32 columns
+constexpr uint32_t kColQ = 128;   // + 64 * t: Q of tile t (bf16 pairs), the A operand of QK^T
 constexpr uint32_t kColO = 256;   // + 128 * t
 
 struct TcMaps {
@@ -74,9 +76,9 @@ struct TcShared {
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s_full[2][2];    // [tile][buffer]: S of a key tile is in TMEM
-    uint64_t p_full[2][2];    // [tile][buffer]: P written over it
-    uint64_t o_done[2];       // PV of a key tile finished accumulating into O
+    uint64_t q_tmem;          // Q rows copied from shared memory into TMEM
+    uint64_t s_full[2];       // [tile]: S of the current key tile is in TMEM
+    uint64_t p_full[2];       // [tile]: P written over it
     uint64_t o_final;
     uint64_t vfix[3];
     uint32_t tmem_base;
@@ -170,14 +172,12 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         mbar_init(bar_addr(sh.q_full), 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_addr(sh.kv_full[s]), 1);
-            mbar_init(bar_addr(sh.kv_empty[s]), g.n_side > 0 ? 2 : 1);
+            mbar_init(bar_addr(sh.kv_empty[s]), g.n_side > 0 ? 5 : 1);   // MMA commit + 4 side warps
         }
+        mbar_init(bar_addr(sh.q_tmem), 128 * g.n_main);
         for (int t = 0; t < 2; ++t) {
-            for (int u = 0; u < 2; ++u) {
-                mbar_init(bar_addr(sh.s_full[t][u]), 1);
-                mbar_init(bar_addr(sh.p_full[t][u]), 128);
-            }
-            mbar_init(bar_addr(sh.o_done[t]), 1);
+            mbar_init(bar_addr(sh.s_full[t]), 1);
+            mbar_init(bar_addr(sh.p_full[t]), 128);
         }
         mbar_init(bar_addr(sh.o_final), 1);
         for (int k = 0; k < 3; ++k) mbar_init(bar_addr(sh.vfix[k]), 1);
@@ -200,6 +200,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         int last_issued[kStages];
 #pragma unroll
         for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
+        int pf_base = -1, pf_page = 0;
         if (lane == 0) {
             prefetch_tmap(&maps.q);
             prefetch_tmap(&maps.kc);
@@ -223,34 +224,48 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             const uint32_t kdst = sStage + s * kStageBytes;
             const uint32_t vdst = kdst + 2 * kHalfBytes;
             const uint32_t full = bar_addr(sh.kv_full[s]);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full, kStageBytes);
-                if (ti.ctx) {
-                    for (int sub = 0; sub < kKeys / box_keys; ++sub) {
-                        const int kk = ti.key0 + sub * box_keys;
-                        int page = p.num_pages;   // past the pool: the box reads zeros
-                        if (kk < g.L) {
-                            page = p.page_table[static_cast<size_t>(g.b) * p.max_pages + kk / p.page_size];
-                            if (page < 0 || page >= p.num_pages) {
-                                report(p.dev_status, DDT_DEV_BAD_PAGE);
-                                page = p.num_pages;
-                            }
-                        }
-                        const int slot_in_page = kk % p.page_size;
-                        for (int h = 0; h < 2; ++h) {
-                            tma_load_4d(kdst + h * kHalfBytes + sub * box_keys * 128, &maps.kc, full,
-                                        64 * h, g.kvh, slot_in_page, page);
-                            tma_load_4d(vdst + h * kHalfBytes + sub * box_keys * 128, &maps.vc, full,
-                                        64 * h, g.kvh, slot_in_page, page);
+            // page ids of the next 32 tiles are fetched by the 32 lanes at once
+            // (one page per tile when pages hold at least 64 keys)
+            int tile_page = p.num_pages;
+            if (ti.ctx && box_keys == kKeys) {
+                if (pf_base < 0 || j >= pf_base + 32) {
+                    pf_base = j;
+                    const int jj = j + lane;
+                    const int kk = (g.t_begin + jj) * kKeys;
+                    pf_page = p.num_pages;
+                    if (jj < g.n_ctx && kk < g.L)
+                        pf_page = p.page_table[static_cast<size_t>(g.b) * p.max_pages + kk / p.page_size];
+                }
+                tile_page = __shfl_sync(0xffffffffu, pf_page, j - pf_base);
+            }
+            mbar_arrive_expect_tx_elect(full, kStageBytes);
+            if (ti.ctx) {
+                for (int sub = 0; sub < kKeys / box_keys; ++sub) {
+                    const int kk = ti.key0 + sub * box_keys;
+                    int page = p.num_pages;   // past the pool: the box reads zeros
+                    if (kk < g.L) {
+                        page = box_keys == kKeys
+                                   ? tile_page
+                                   : p.page_table[static_cast<size_t>(g.b) * p.max_pages + kk / p.page_size];
+                        if (page < 0 || page >= p.num_pages) {
+                            if (lane == 0) report(p.dev_status, DDT_DEV_BAD_PAGE);
+                            page = p.num_pages;
                         }
                     }
-                } else {
+                    const int slot_in_page = kk % p.page_size;
                     for (int h = 0; h < 2; ++h) {
-                        tma_load_3d(kdst + h * kHalfBytes, &maps.kt, full, 64 * h, g.kvh,
-                                    g.b * p.N + ti.key0);
-                        tma_load_3d(vdst + h * kHalfBytes, &maps.vt, full, 64 * h, g.kvh,
-                                    g.b * p.N + ti.key0);
+                        tma_load_4d_elect(kdst + h * kHalfBytes + sub * box_keys * 128, &maps.kc, full,
+                                          64 * h, g.kvh, slot_in_page, page);
+                        tma_load_4d_elect(vdst + h * kHalfBytes + sub * box_keys * 128, &maps.vc, full,
+                                          64 * h, g.kvh, slot_in_page, page);
                     }
+                }
+            } else {
+                for (int h = 0; h < 2; ++h) {
+                    tma_load_3d_elect(kdst + h * kHalfBytes, &maps.kt, full, 64 * h, g.kvh,
+                                      g.b * p.N + ti.key0);
+                    tma_load_3d_elect(vdst + h * kHalfBytes, &maps.vt, full, 64 * h, g.kvh,
+                                      g.b * p.N + ti.key0);
                 }
             }
             last_issued[s] = j;
@@ -279,61 +294,67 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        // The whole warp runs this loop so every operand is warp-uniform; one
+        // elected lane issues each tcgen05 instruction.
+        {
             const uint32_t id_s = idesc_bf16_f32(128, kKeys, 0, 0);
             const uint32_t id_o = idesc_bf16_f32(128, kD, 0, 1);
-            // S_t[j % 2] = Q_t K_j^T
+            // Descriptors: one base per operand; an MMA only adds its byte offset >> 4
+            // to the start-address field (addresses stay below 256 KB, so no carry).
+            const uint64_t dq = smem_desc(sQ, 16, 1024);
+            const uint64_t dk = smem_desc(sStage, 16, 1024);
+            const uint64_t dv = smem_desc(sStage + 2 * kHalfBytes, kHalfBytes, 1024);
+            // S_t = Q_t K_j^T (Q from TMEM)
             auto qk = [&](int t, int j) {
-                const uint32_t kb = sStage + (j % kStages) * kStageBytes;
-                const uint32_t d = tbase + kColS + 64 * (2 * t + (j & 1));
+                const uint32_t koff = ((j % kStages) * kStageBytes) >> 4;
+                const uint32_t d = tbase + kColS + 64 * t;
+                const uint32_t qa = tbase + kColQ + 64 * t;
 #pragma unroll
                 for (int ks = 0; ks < kD / 16; ++ks) {
-                    const uint32_t a = sQ + t * kQTileBytes + (ks / 4) * (kQTileBytes / 2) + (ks % 4) * 32;
-                    const uint32_t bk = kb + (ks / 4) * kHalfBytes + (ks % 4) * 32;
-                    mma_ss(d, smem_desc(a, 16, 1024), smem_desc(bk, 16, 1024), id_s, ks > 0);
+                    const uint32_t ko = koff + (((ks / 4) * kHalfBytes + (ks % 4) * 32) >> 4);
+                    mma_ts_elect(d, qa + 8 * ks, dk + ko, id_s, ks > 0);
                 }
-                mma_commit(bar_addr(sh.s_full[t][j & 1]));
+                mma_commit_elect(bar_addr(sh.s_full[t]));
             };
-            // O_t (+)= P_t[j % 2] V_j
+            // O_t (+)= P_t V_j
             auto pv = [&](int t, int j) {
-                const uint32_t vb = sStage + (j % kStages) * kStageBytes + 2 * kHalfBytes;
-                const uint32_t a = tbase + kColS + 64 * (2 * t + (j & 1));
+                const uint32_t voff = ((j % kStages) * kStageBytes) >> 4;
+                const uint32_t a = tbase + kColS + 64 * t;
+                const uint32_t o = tbase + kColO + 128 * t;
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    mma_ts(tbase + kColO + 128 * t, a + 8 * ks, smem_desc(vb + ks * 2048, kHalfBytes, 1024),
-                           id_o, (j > 0) || ks > 0);
-                mma_commit(bar_addr(sh.o_done[t]));
+                    mma_ts_elect(o, a + 8 * ks, dv + voff + ((ks * 2048) >> 4), id_o, (j > 0) || ks > 0);
             };
-            auto k_ready = [&](int j) {
-                return mbar_wait_bounded(bar_addr(sh.kv_full[j % kStages]), (j / kStages) & 1, abort);
+            auto wait_all = [&](uint32_t bar, uint32_t parity) {
+                return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort));
             };
-            bool ok = mbar_wait_bounded(bar_addr(sh.q_full), 0, abort);
-            // prologue: S for key tiles 0 and 1
-            for (int j = 0; ok && j < 2 && j < g.n_tiles; ++j) {
-                if (!k_ready(j)) { ok = false; break; }
+            bool ok = wait_all(bar_addr(sh.q_tmem), 0) && (g.n_tiles == 0 || wait_all(bar_addr(sh.kv_full[0]), 0));
+            if (ok && g.n_tiles > 0) {
                 tc_fence_after();
-                qk(0, j);
-                if (g.n_main == 2) qk(1, j);
+                qk(0, 0);
+                if (g.n_main == 2) qk(1, 0);
             }
             for (int j = 0; ok && j < g.n_tiles; ++j) {
                 const TileInfo ti = tile_info(g, j);
-                if (ti.fix >= 0 && !mbar_wait_bounded(bar_addr(sh.vfix[ti.fix]), 0, abort)) break;
-                bool go = true;
-                for (int t = 0; t < g.n_main; ++t) {
-                    if (!mbar_wait_bounded(bar_addr(sh.p_full[t][j & 1]), (j >> 1) & 1, abort)) { go = false; break; }
+                const bool more = j + 1 < g.n_tiles;
+                if (ti.fix >= 0 && !wait_all(bar_addr(sh.vfix[ti.fix]), 0)) break;
+                if (!wait_all(bar_addr(sh.p_full[0]), j & 1)) break;
+                tc_fence_after();
+                pv(0, j);
+                if (more) {
+                    if (!wait_all(bar_addr(sh.kv_full[(j + 1) % kStages]), ((j + 1) / kStages) & 1)) break;
                     tc_fence_after();
-                    pv(t, j);
+                    qk(0, j + 1);   // after PV_0(j) in issue order, so P_0 is consumed first
                 }
-                if (!go) break;
-                mma_commit(bar_addr(sh.kv_empty[j % kStages]));   // K_j and V_j consumed
-                if (j + 2 < g.n_tiles) {
-                    if (!k_ready(j + 2)) break;
+                if (g.n_main == 2) {
+                    if (!wait_all(bar_addr(sh.p_full[1]), j & 1)) break;
                     tc_fence_after();
-                    qk(0, j + 2);
-                    if (g.n_main == 2) qk(1, j + 2);
+                    pv(1, j);
                 }
+                mma_commit_elect(bar_addr(sh.kv_empty[j % kStages]));   // K_j and V_j consumed
+                if (g.n_main == 2 && more) qk(1, j + 1);
             }
-            mma_commit(bar_addr(sh.o_final));
+            mma_commit_elect(bar_addr(sh.o_final));
             mbar_drain(bar_addr(sh.o_final), 0);   // every MMA done before TMEM is freed
         }
         __syncwarp();
@@ -351,20 +372,38 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         if (real)
             for (int w = 0; w < p.W; ++w) visw[w] = p.vis[(static_cast<size_t>(g.b) * p.N + node) * p.W + w];
         const uint32_t lane_off = static_cast<uint32_t>(32 * qw) << 16;
-        const uint32_t tS0 = tbase + lane_off + kColS + 64 * (2 * t);
+        const uint32_t tS = tbase + lane_off + kColS + 64 * t;
         const uint32_t tO = tbase + lane_off + kColO + 128 * t;
+        // copy this thread's Q row (TMA-written, 128-byte swizzled) into TMEM
+        if (active) {
+            const bool q_ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.q_full), 0, abort));
+            const unsigned char* qrow = smem + kOffQ + t * kQTileBytes;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t w[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = q_ok ? *reinterpret_cast<const uint4*>(
+                                               qrow + hh * (kQTileBytes / 2) + sw128_offset(row_local, c))
+                                         : make_uint4(0, 0, 0, 0);
+                    w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+                }
+                tmem_st32(tbase + lane_off + kColQ + 64 * t + 32 * hh, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar_addr(sh.q_tmem));
+        }
         const float sc = p.scale_log2;            // > 0 on this path
         float m_ref = -INFINITY;                  // reference max, scaled log2 units
         float l_sum = 0.0f;
         bool ok = active;
         for (int j = 0; ok && j < g.n_tiles; ++j) {
-            const int u = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.s_full[t][u]), (j >> 1) & 1, abort))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.s_full[t]), j & 1, abort))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t tS = tS0 + 64 * u;
             uint32_t raw[2][32];
             tmem_ld32(tS, raw[0]);
             tmem_ld32(tS + 32, raw[1]);
@@ -402,12 +441,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             const float mxs = mx * sc;
             if (mxs > m_ref + 8.0f) {   // raise the reference: rescale O and l
                 if (j > 0 && m_ref != -INFINITY) {
-                    // O must hold every earlier key tile before it is rescaled
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait_bounded(bar_addr(sh.o_done[t]), (j - 1) & 1, abort))) {
-                        ok = false;
-                    }
-                    tc_fence_after();
+                    // QK_t(j) was issued after PV_t(j-1), so S ready means O is complete
                     const float alpha = fast_exp2(m_ref - mxs);
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -437,7 +471,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             tmem_st32(tS, raw[0]);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_addr(sh.p_full[t][u]));
+            mbar_arrive(bar_addr(sh.p_full[t]));
         }
         if (active) {
             const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.o_final), 0, abort));
@@ -525,30 +559,32 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
 #pragma unroll
         for (int mb = 0; mb < kD / 16; ++mb) oacc[mb][0] = oacc[mb][1] = oacc[mb][2] = oacc[mb][3] = 0.0f;
         bool ok = true;
+        // Each of the four warps runs its own online softmax over its 16 keys of
+        // every tile; the four partial results are merged once at the end.
         for (int j = 0; j < g.n_tiles; ++j) {
             const int s = j % kStages;
             const TileInfo ti = tile_info(g, j);
-            bool got = mbar_wait_bounded(bar_addr(sh.kv_full[s]), (j / kStages) & 1, abort);
+            bool got = ok && mbar_wait_bounded(bar_addr(sh.kv_full[s]), (j / kStages) & 1, abort);
             if (got && ti.fix >= 0) got = mbar_wait_bounded(bar_addr(sh.vfix[ti.fix]), 0, abort);
-            if (!__all_sync(0xffffffffu, got)) ok = false;
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             const unsigned char* kst = smem + kOffStages + s * kStageBytes;
             const unsigned char* vst = kst + 2 * kHalfBytes;
-            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (ok) {
+            // S^T (16 keys x 8 rows) = K Q^T, two accumulators to halve the dependency chain
+            float c[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int ks = 0; ks < kD / 16; ++ks) {
-                    const int key = 16 * sw + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int chunk = ks * 2 + (lane >> 4);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(smem_u32(kst + (chunk >> 3) * kHalfBytes + sw128_offset(key, chunk & 7)),
-                            a0, a1, a2, a3);
-                    mma16816(c, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-                }
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const int key = 16 * sw + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int chunk = ks * 2 + (lane >> 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(smem_u32(kst + (chunk >> 3) * kHalfBytes + sw128_offset(key, chunk & 7)), a0, a1, a2, a3);
+                if (ks & 1) mma16816(c2, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                else mma16816(c, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
             // scale, mask; c0/c1: key kA rows crow0/crow0+1; c2/c3: key kA+8
             const int kA = 16 * sw + nrow;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
+                c[e] += c2[e];
                 const int kl = kA + ((e >> 1) << 3);
                 const int q = e & 1;
                 bool vis_ok = node_r[q] >= 0 && kl < ti.valid;
@@ -556,34 +592,23 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                     const int key = ti.key0 + kl;
                     vis_ok = (pick4(visr[q], key >> 5) >> (key & 31)) & 1u;
                 }
-                c[e] = (ok && vis_ok) ? c[e] * p.scale_log2 : -INFINITY;
+                c[e] = vis_ok ? c[e] * p.scale_log2 : -INFINITY;
             }
             float mx[2] = {fmaxf(c[0], c[2]), fmaxf(c[1], c[3])};
+            float alpha[2], m_use[2];
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 4));
                 mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 8));
                 mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 16));
-            }
-            if (lane < 4) {
-                sh.side_max[j & 1][sw][crow0] = mx[0];
-                sh.side_max[j & 1][sw][crow0 + 1] = mx[1];
-            }
-            named_bar_sync(1, 128);
-            float alpha[2], m_use[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                float tm = sh.side_max[j & 1][0][crow0 + q];
-#pragma unroll
-                for (int w = 1; w < 4; ++w) tm = fmaxf(tm, sh.side_max[j & 1][w][crow0 + q]);
-                const float m_new = fmaxf(m_run[q], tm);
+                const float m_new = fmaxf(m_run[q], mx[q]);
                 m_use[q] = (m_new == -INFINITY) ? 0.0f : m_new;
-                alpha[q] = exp2f(m_run[q] - m_use[q]);
+                alpha[q] = fast_exp2(m_run[q] - m_use[q]);
                 m_run[q] = m_new;
             }
             float pe[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) pe[e] = exp2f(c[e] - m_use[e & 1]);
+            for (int e = 0; e < 4; ++e) pe[e] = fast_exp2(c[e] - m_use[e & 1]);
             l_part[0] = l_part[0] * alpha[0] + pe[0] + pe[2];
             l_part[1] = l_part[1] * alpha[1] + pe[1] + pe[3];
 #pragma unroll
@@ -595,45 +620,51 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             __nv_bfloat162 p23 = __floats2bfloat162_rn(pe[2], pe[3]);
             const uint32_t b0 = movmatrix_t(*reinterpret_cast<uint32_t*>(&p01));
             const uint32_t b1 = movmatrix_t(*reinterpret_cast<uint32_t*>(&p23));
-            if (ok) {
 #pragma unroll
-                for (int mb = 0; mb < kD / 16; ++mb) {
-                    const int key = 16 * sw + (lane & 7) + (lane >> 4) * 8;
-                    const int chunk = mb * 2 + ((lane >> 3) & 1);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4_t(smem_u32(vst + (chunk >> 3) * kHalfBytes + sw128_offset(key, chunk & 7)),
-                              a0, a1, a2, a3);
-                    mma16816(oacc[mb], a0, a1, a2, a3, b0, b1);
-                }
+            for (int mb = 0; mb < kD / 16; ++mb) {
+                const int key = 16 * sw + (lane & 7) + (lane >> 4) * 8;
+                const int chunk = mb * 2 + ((lane >> 3) & 1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(smem_u32(vst + (chunk >> 3) * kHalfBytes + sw128_offset(key, chunk & 7)), a0, a1, a2, a3);
+                mma16816(oacc[mb], a0, a1, a2, a3, b0, b1);
             }
-            named_bar_sync(1, 128);
-            if (sw == 0 && lane == 0 && ok) mbar_arrive(bar_addr(sh.kv_empty[s]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(sh.kv_empty[s]));   // this warp is done with the stage
         }
-        // combine the four warps' partial sums (each covers its 16 keys of every tile)
-        float* side_o = reinterpret_cast<float*>(smem + kOffSideO);   // [kD][kMaxSide]
-        for (int x = tid - 384; x < kD * kMaxSide; x += 128) side_o[x] = 0.0f;
+        // merge the four warps: common max per row, then rescaled sums
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             l_part[q] += __shfl_xor_sync(0xffffffffu, l_part[q], 4);
             l_part[q] += __shfl_xor_sync(0xffffffffu, l_part[q], 8);
             l_part[q] += __shfl_xor_sync(0xffffffffu, l_part[q], 16);
         }
+        float* side_o = reinterpret_cast<float*>(smem + kOffSideO);   // [kD][kMaxSide]
+        for (int x = tid - 384; x < kD * kMaxSide; x += 128) side_o[x] = 0.0f;
         if (lane < 4) {
-            sh.side_l[sw][crow0] = l_part[0];
-            sh.side_l[sw][crow0 + 1] = l_part[1];
-            if (sw == 0) {
-                sh.side_m[crow0] = m_run[0];
-                sh.side_m[crow0 + 1] = m_run[1];
-            }
+            sh.side_max[0][sw][crow0] = m_run[0];
+            sh.side_max[0][sw][crow0 + 1] = m_run[1];
         }
         named_bar_sync(1, 128);
+        float wscale[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            float M = sh.side_max[0][0][crow0 + q];
+#pragma unroll
+            for (int w2 = 1; w2 < 4; ++w2) M = fmaxf(M, sh.side_max[0][w2][crow0 + q]);
+            wscale[q] = (M == -INFINITY) ? 0.0f : fast_exp2(m_run[q] - M);
+            if (sw == 0 && lane < 4) sh.side_m[crow0 + q] = M;
+        }
+        if (lane < 4) {
+            sh.side_l[sw][crow0] = l_part[0] * wscale[0];
+            sh.side_l[sw][crow0 + 1] = l_part[1] * wscale[1];
+        }
 #pragma unroll
         for (int mb = 0; mb < kD / 16; ++mb) {
             const int d0 = 16 * mb + nrow;
-            atomicAdd(&side_o[d0 * kMaxSide + crow0], oacc[mb][0]);
-            atomicAdd(&side_o[d0 * kMaxSide + crow0 + 1], oacc[mb][1]);
-            atomicAdd(&side_o[(d0 + 8) * kMaxSide + crow0], oacc[mb][2]);
-            atomicAdd(&side_o[(d0 + 8) * kMaxSide + crow0 + 1], oacc[mb][3]);
+            atomicAdd(&side_o[d0 * kMaxSide + crow0], oacc[mb][0] * wscale[0]);
+            atomicAdd(&side_o[d0 * kMaxSide + crow0 + 1], oacc[mb][1] * wscale[1]);
+            atomicAdd(&side_o[(d0 + 8) * kMaxSide + crow0], oacc[mb][2] * wscale[0]);
+            atomicAdd(&side_o[(d0 + 8) * kMaxSide + crow0 + 1], oacc[mb][3] * wscale[1]);
         }
         named_bar_sync(1, 128);
         // write: thread -> (row tid/16, 8 features)
@@ -643,7 +674,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             const int r = 256 + sr;
             const int i = r / g.G, h = g.kvh * g.G + r % g.G;
             const float lt = sh.side_l[0][sr] + sh.side_l[1][sr] + sh.side_l[2][sr] + sh.side_l[3][sr];
-            const float mrun = sh.side_m[sr];   // the same in every side warp
+            const float mrun = sh.side_m[sr];
             const bool real = i < g.nn && ok;
             if (!split) {
                 const float inv = (real && lt > 0.0f) ? 1.0f / lt : 0.0f;

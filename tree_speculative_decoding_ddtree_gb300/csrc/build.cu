@@ -8,16 +8,17 @@
 // Context section (top-k cap per node) and Hypothesis 3 (position =
 // ctx_len + depth).
 //
-// GPU design: the frontier (the heap's contents) lives in shared memory as a
-// flat array of at most budget+1 live entries; each pop is a warp-wide argmax
-// over (score desc, push sequence asc), which is the heap's total order, so
-// the pop sequence is the heap's exactly. Removal moves the last entry into
-// the hole. Scores are fp64 sums in path order, as in the definition.
+// GPU design: one warp (one CTA) per request. The request's per-depth top-k is
+// staged in shared memory first, so the serial pop loop never waits on global
+// memory. The frontier (the heap's contents) lives in shared memory as a flat
+// array of at most budget+1 live entries; each pop is a warp-wide argmax over
+// (score desc, push sequence asc), which is the heap's total order, so the pop
+// sequence is the heap's exactly. Removal moves the last entry into the hole.
+// Scores are fp64 sums in path order, as in the definition.
 #include "common.cuh"
 
 namespace ddt {
 
-constexpr int kBuildWarps = 4;
 constexpr int kMaxN = DDT_MAX_NODES;          // 128
 constexpr int kMaxW = (kMaxN + 31) / 32;      // 4
 constexpr int kMaxFrontier = kMaxN;           // live entries <= 1 + budget <= 128
@@ -44,7 +45,7 @@ DDT_DEVINL bool pops_before(double s, int q, double bs, int bq) {
     return s > bs || (s == bs && q < bq);
 }
 
-__global__ void __launch_bounds__(32 * kBuildWarps)
+__global__ void __launch_bounds__(32)
 ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restrict__ topk_tok,
                     const int32_t* __restrict__ root_tok, const int32_t* __restrict__ ctx_len,
                     int B, int D, int K, int budget,
@@ -54,14 +55,18 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
                     int32_t* __restrict__ first_child, int32_t* __restrict__ next_sibling,
                     uint32_t* __restrict__ vis, int32_t* __restrict__ n_nodes_out,
                     int32_t* dev_status) {
-    __shared__ BuildSmem smem_all[kBuildWarps];
-    const int warp = threadIdx.x >> 5;
+    __shared__ BuildSmem s;
+    extern __shared__ unsigned char dyn[];     // staged top-k: D*K floats then D*K ints
     const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * kBuildWarps + warp;
-    if (b >= B) return;
-    BuildSmem& s = smem_all[warp];
-    const float* lp = topk_logp + static_cast<size_t>(b) * D * K;
-    const int32_t* tk = topk_tok + static_cast<size_t>(b) * D * K;
+    const int b = blockIdx.x;
+    float* lp = reinterpret_cast<float*>(dyn);
+    int32_t* tk = reinterpret_cast<int32_t*>(dyn + sizeof(float) * D * K);
+    {
+        const float* glp = topk_logp + static_cast<size_t>(b) * D * K;
+        const int32_t* gtk = topk_tok + static_cast<size_t>(b) * D * K;
+        for (int x = lane; x < D * K; x += 32) { lp[x] = glp[x]; tk[x] = gtk[x]; }
+        __syncwarp();
+    }
     const int N = budget + 1;
     const int W = (N + 31) >> 5;
 
@@ -185,8 +190,8 @@ cudaError_t launch_build(const float* topk_logp, const int32_t* topk_tok, const 
                          int32_t* pos, double* score, int32_t* first_child,
                          int32_t* next_sibling, uint32_t* vis, int32_t* n_nodes,
                          int32_t* dev_status, cudaStream_t stream) {
-    const dim3 grid((B + kBuildWarps - 1) / kBuildWarps);
-    ddtree_build_kernel<<<grid, 32 * kBuildWarps, 0, stream>>>(
+    const size_t dyn = static_cast<size_t>(D) * K * 8;
+    ddtree_build_kernel<<<B, 32, dyn, stream>>>(
         topk_logp, topk_tok, root_tok, ctx_len, B, D, K, budget, parent, depth, token, rank,
         pos, score, first_child, next_sibling, vis, n_nodes, dev_status);
     return cudaGetLastError();

@@ -47,28 +47,37 @@ TC_DEVINL uint64_t globaltimer_ns() {
 }
 
 // Bounded wait on a barrier phase. Returns false (and sets *abort) if the
-// phase does not complete within `limit_ns`, or at once if *abort is set.
+// phase does not complete within about `limit_ns`, or at once if *abort is
+// set. The clock is read only after 1024 unsuccessful polls, so short
+// handoffs never pay for a timer read.
 TC_DEVINL bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                  uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (*abort) return false;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) {
-            *abort = 1;
-            return false;
+        if (*abort) return false;
+        if ((it & 1023u) == 1023u) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                *abort = 1;
+                return false;
+            }
         }
     }
 }
 
 // The same, ignoring the abort flag (used to drain copies and MMAs in flight).
 TC_DEVINL bool mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+        if ((it & 1023u) == 1023u) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > limit_ns) return false;
+        }
     }
 }
 
@@ -90,6 +99,30 @@ TC_DEVINL void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
            "r"(c3)
         : "memory");
+}
+// warp-converged variants: one elected lane issues
+TC_DEVINL void tma_load_3d_elect(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2) {
+    asm volatile(
+        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+        " @p cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];\n}\n"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+TC_DEVINL void tma_load_4d_elect(uint32_t dst, const void* tmap, uint32_t bar, int c0, int c1, int c2,
+                                 int c3) {
+    asm volatile(
+        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+        " @p cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];\n}\n"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
+           "r"(c3)
+        : "memory");
+}
+TC_DEVINL void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n .reg .pred p;\n .reg .b64 st;\n elect.sync _|p, 0xffffffff;\n"
+                 " @p mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n"
+                 :: "r"(bar), "r"(bytes) : "memory");
 }
 TC_DEVINL void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];\n" :: "l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -190,6 +223,28 @@ TC_DEVINL void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_
                  :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
                  : "memory");
 }
+// Warp-converged variants: every lane of the warp executes the call with the
+// same operands and one elected lane issues the instruction.
+TC_DEVINL void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                            uint32_t accumulate) {
+    asm volatile("{\n .reg .pred p, q;\n elect.sync _|p, 0xffffffff;\n setp.ne.b32 q, %4, 0;\n"
+                 " @p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n}\n"
+                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+TC_DEVINL void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                            uint32_t accumulate) {
+    asm volatile("{\n .reg .pred p, q;\n elect.sync _|p, 0xffffffff;\n setp.ne.b32 q, %4, 0;\n"
+                 " @p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n}\n"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+TC_DEVINL void mma_commit_elect(uint32_t bar) {
+    asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+                 " @p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n"
+                 :: "r"(bar) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread completes.
 TC_DEVINL void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
