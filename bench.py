@@ -336,28 +336,55 @@ def run_native(args):
               bonus=torch.empty(w.B, dtype=torch.int32, device=device))
     so = {k: torch.empty_like(t) for k, t in go.items()}
     scale = 1.0 / math.sqrt(w.Dh)
-    attn_events = []
 
-    def step(timed=False):
+    def step():
         dd.ddtree_build(topk_logp, topk_tok, root, ctx, w.budget, out=tree, dev_status=status)
-        if timed:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
         dd.tree_verify_attn(q, k_tree, v_tree, k_cache, v_cache, table, ctx, tree.vis, tree.n_nodes,
                             scale, out=out, workspace=workspace, dev_status=status)
-        if timed:
-            e1.record(stream)
-            attn_events.append((e0, e1))
         dd.ddtree_accept_greedy(logits, tree, w.D, out=go, dev_status=status)
         dd.ddtree_accept_sample(logits, tree, w.D, temp, seed, 0, out=so, dev_status=status)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    # The step is replayed as one CUDA graph (the four calls allocate nothing and
+    # never synchronise, so they capture as they are); this removes the host's
+    # per-call launch overhead from the device timeline.
+    cap_stream = torch.cuda.Stream(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap_stream):
+        with torch.cuda.graph(graph, stream=cap_stream):
+            step()
+    torch.cuda.synchronize()
+
+    def graph_of(fn, reps):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(gr, stream=cap_stream):
+                for _ in range(reps):
+                    fn()
+        return gr
+
+    calls = {
+        "ddtree_build": lambda: dd.ddtree_build(topk_logp, topk_tok, root, ctx, w.budget, out=tree,
+                                                dev_status=status),
+        "tree_verify_attn": lambda: dd.tree_verify_attn(q, k_tree, v_tree, k_cache, v_cache, table, ctx,
+                                                        tree.vis, tree.n_nodes, scale, out=out,
+                                                        workspace=workspace, dev_status=status),
+        "ddtree_accept_greedy": lambda: dd.ddtree_accept_greedy(logits, tree, w.D, out=go, dev_status=status),
+        "ddtree_accept_sample": lambda: dd.ddtree_accept_sample(logits, tree, w.D, temp, seed, 0, out=so,
+                                                                dev_status=status),
+    }
+    call_graphs = {n: graph_of(f, 10) for n, f in calls.items()}
+    torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
             dist.barrier()
 
     for _ in range(max(args.warmup, 3)):
-        step()
+        graph.replay()
     torch.cuda.synchronize()
     barrier()
     launches_per_step = 4 + (1 if ws_bytes > 0 else 0)
@@ -368,12 +395,33 @@ def run_native(args):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for _ in range(args.steps):
-            step(timed=True)
+            graph.replay()
         t_end.record(stream)
         torch.cuda.synchronize()
         barrier()
+        # tree_verify_attn alone, back to back on the same stream (roofline timing)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        attn_reps = max(20, args.steps // 10)
+        a0.record(stream)
+        for _ in range(attn_reps // 10):
+            call_graphs["tree_verify_attn"].replay()
+        a1.record(stream)
+        torch.cuda.synchronize()
     elapsed_ms = t_start.elapsed_time(t_end)
-    attn_ms = [a.elapsed_time(b) for a, b in attn_events]
+    attn_avg_ms = a0.elapsed_time(a1) / ((attn_reps // 10) * 10)
+    per_call_us = {}
+    for n, gr in call_graphs.items():
+        gr.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        per_call_us[n] = e0.elapsed_time(e1) * 1e3 / 50
     if world > 1:
         tt = torch.tensor([elapsed_ms], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -426,7 +474,6 @@ def run_native(args):
         peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
         ms_per_step = elapsed_ms / args.steps
         value = world * args.steps / (elapsed_ms / 1e3)
-        attn_avg_ms = sum(attn_ms) / len(attn_ms)
         abytes = algorithmic_attn_bytes(w, h["ctx"])
         aflops = algorithmic_attn_flops(w, h["ctx"], depth_sum)
         achieved = abytes / (attn_avg_ms * 1e-3) / 1e9
@@ -451,6 +498,7 @@ def run_native(args):
             "e2e": {"value": world * args.e2e_steps / e2e_s, "unit": "steps/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "note": "KV cache stays resident (it is the cache); all per-step inputs copied in"},
+            "per_call_us": per_call_us,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }

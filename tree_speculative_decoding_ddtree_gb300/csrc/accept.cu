@@ -107,12 +107,30 @@ struct WalkOut {
     int32_t* bonus;
 };
 
+// The request's token / first-child / next-sibling rows, staged in shared
+// memory so the serial child scans never wait on global memory.
+struct TreeRows {
+    int tok[DDT_MAX_NODES];
+    int fc[DDT_MAX_NODES];
+    int ns[DDT_MAX_NODES];
+};
+
+DDT_DEVINL void stage_tree(TreeRows& t, const int32_t* token, const int32_t* first_child,
+                           const int32_t* next_sibling, size_t tb, int N) {
+    for (int i = threadIdx.x; i < N; i += kAcceptThreads) {
+        t.tok[i] = token[tb + i];
+        t.fc[i] = first_child[tb + i];
+        t.ns[i] = next_sibling[tb + i];
+    }
+}
+
 __global__ void __launch_bounds__(kAcceptThreads)
 accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
                      const int32_t* __restrict__ token, const int32_t* __restrict__ first_child,
                      const int32_t* __restrict__ next_sibling, const int32_t* __restrict__ n_nodes,
                      int N, int D, WalkOut o, int32_t* dev_status) {
     __shared__ unsigned long long scratch[32];
+    __shared__ TreeRows tr;
     __shared__ int s_next;
     __shared__ int s_len;
     const int b = blockIdx.x;
@@ -120,6 +138,7 @@ accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
     int32_t* toks = o.out_tokens + static_cast<size_t>(b) * (D + 1);
     int32_t* nodes = o.out_nodes + static_cast<size_t>(b) * (D + 1);
     for (int k = threadIdx.x; k <= D; k += kAcceptThreads) { toks[k] = -1; nodes[k] = -1; }
+    stage_tree(tr, token, first_child, next_sibling, tb, N);
     int nn = n_nodes[b];
     if (nn < 1 || nn > N) {
         if (threadIdx.x == 0) report(dev_status, DDT_DEV_BAD_TREE);
@@ -132,16 +151,16 @@ accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
     while (true) {
         const uint32_t a = row_argmax(logits + (tb + u) * static_cast<size_t>(V), V, vec4, scratch);
         if (threadIdx.x == 0) {
-            int match = -1, c = first_child[tb + u], guard = 0;
+            int match = -1, c = tr.fc[u], guard = 0;
             while (c != -1) {
                 if (c < 1 || c >= nn || ++guard > kMaxKids) { report(dev_status, DDT_DEV_BAD_TREE); break; }
-                if (token[tb + c] == static_cast<int32_t>(a)) { match = c; break; }
-                c = next_sibling[tb + c];
+                if (tr.tok[c] == static_cast<int32_t>(a)) { match = c; break; }
+                c = tr.ns[c];
             }
-            int len = s_len;
+            const int len = s_len;
             if (match != -1 && len >= D) { report(dev_status, DDT_DEV_BAD_TREE); match = -1; }
             if (match != -1) {
-                toks[len] = token[tb + match];
+                toks[len] = tr.tok[match];
                 nodes[len + 1] = match;
                 s_len = len + 1;
             } else {
@@ -157,6 +176,11 @@ accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
     }
 }
 
+// online (max, sum of exp((x - max) / T)) pair, merged in a block reduction
+struct MaxSum {
+    float m, z;
+};
+
 __global__ void __launch_bounds__(kAcceptThreads)
 accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
                      const int32_t* __restrict__ token, const int32_t* __restrict__ first_child,
@@ -165,8 +189,13 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
                      const uint64_t* __restrict__ seed, uint64_t offset, WalkOut o,
                      int32_t* dev_status) {
     __shared__ unsigned long long scratch_u[32];
-    __shared__ float scratch_f[32];
+    __shared__ float scratch_m[32];
+    __shared__ float scratch_z[32];
+    __shared__ TreeRows tr;
     __shared__ int s_kid_tok[kMaxKids];
+    __shared__ int s_kid_node[kMaxKids];
+    __shared__ float s_q[kMaxKids];
+    __shared__ double s_u[kMaxKids];
     __shared__ int s_nkids;
     __shared__ int s_next;
     __shared__ int s_len;
@@ -175,6 +204,7 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     int32_t* toks = o.out_tokens + static_cast<size_t>(b) * (D + 1);
     int32_t* nodes = o.out_nodes + static_cast<size_t>(b) * (D + 1);
     for (int k = threadIdx.x; k <= D; k += kAcceptThreads) { toks[k] = -1; nodes[k] = -1; }
+    stage_tree(tr, token, first_child, next_sibling, tb, N);
     int nn = n_nodes[b];
     if (nn < 1 || nn > N) {
         if (threadIdx.x == 0) report(dev_status, DDT_DEV_BAD_TREE);
@@ -199,74 +229,103 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     int u = 0;
     while (true) {
         const float* row = logits + (tb + u) * static_cast<size_t>(V);
-        // pass 1: max; pass 2: softmax denominator of logits / T
-        float m = -INFINITY;
-        if (vec4) {
-            const float4* r4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 8
-            for (int x = threadIdx.x; x < (V >> 2); x += kAcceptThreads) {
-                const float4 f = __ldg(r4 + x);
-                m = fmaxf(m, fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)));
-            }
-        } else {
-            for (int v = threadIdx.x; v < V; v += kAcceptThreads) m = fmaxf(m, __ldg(row + v));
-        }
-        m = block_reduce(m, scratch_f, MaxF(), -INFINITY);
-        float z = 0.0f;
-        if (vec4) {
-            const float4* r4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 8
-            for (int x = threadIdx.x; x < (V >> 2); x += kAcceptThreads) {
-                const float4 f = __ldg(r4 + x);
-                z += expf((f.x - m) * inv_t) + expf((f.y - m) * inv_t) +
-                     expf((f.z - m) * inv_t) + expf((f.w - m) * inv_t);
-            }
-        } else {
-            for (int v = threadIdx.x; v < V; v += kAcceptThreads) z += expf((__ldg(row + v) - m) * inv_t);
-        }
-        z = block_reduce(z, scratch_f, SumF(), 0.0f);
-        // children in rank order: accept child j when u_j * R < q(x_j)
+        // the node's children, in rank order (thread 0, from shared memory)
         if (threadIdx.x == 0) {
-            int match = -1, c = first_child[tb + u], j = 0;
-            double R = 1.0;
+            int c = tr.fc[u], j = 0;
             while (c != -1) {
                 if (c < 1 || c >= nn || j >= kMaxKids) { report(dev_status, DDT_DEV_BAD_TREE); break; }
-                const int x = token[tb + c];
-                s_kid_tok[j] = x;
-                float q = 0.0f;
-                if (x >= 0 && x < V) q = expf((row[x] - m) * inv_t) / z;
-                else report(dev_status, DDT_DEV_BAD_TOKEN);
-                const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(u),
-                                                         static_cast<uint32_t>(j), off_lo), k0, k1);
+                s_kid_node[j] = c;
+                s_kid_tok[j] = tr.tok[c];
                 ++j;
-                if (uniform_exact(w.x) * R < static_cast<double>(q)) { match = c; break; }
-                R -= static_cast<double>(q);
-                c = next_sibling[tb + c];
+                c = tr.ns[c];
             }
-            if (match == -1) {   // finish the child list so the bonus excludes every child
-                int guard = j;
-                while (c != -1 && guard < kMaxKids) {
-                    if (c < 1 || c >= nn) { report(dev_status, DDT_DEV_BAD_TREE); break; }
-                    s_kid_tok[guard++] = token[tb + c];
-                    c = next_sibling[tb + c];
+            s_nkids = j;
+        }
+        // one pass: running max and softmax denominator of logits / T
+        float m = -INFINITY, z = 0.0f;
+        auto add = [&](float x) {
+            if (x > m) {
+                z = z * expf((m - x) * inv_t) + 1.0f;
+                m = x;
+            } else {
+                z += expf((x - m) * inv_t);
+            }
+        };
+        if (vec4) {
+            const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 8
+            for (int x = threadIdx.x; x < (V >> 2); x += kAcceptThreads) {
+                const float4 f = __ldg(r4 + x);
+                add(f.x); add(f.y); add(f.z); add(f.w);
+            }
+        } else {
+            for (int v = threadIdx.x; v < V; v += kAcceptThreads) add(__ldg(row + v));
+        }
+        {
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+                const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
+                const float M = fmaxf(m, m2);
+                z = (M == -INFINITY) ? 0.0f : z * expf((m - M) * inv_t) + z2 * expf((m2 - M) * inv_t);
+                m = M;
+            }
+            __syncthreads();
+            if (lane == 0) { scratch_m[warp] = m; scratch_z[warp] = z; }
+            __syncthreads();
+            if (warp == 0) {
+                m = lane < kAcceptThreads / 32 ? scratch_m[lane] : -INFINITY;
+                z = lane < kAcceptThreads / 32 ? scratch_z[lane] : 0.0f;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+                    const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
+                    const float M = fmaxf(m, m2);
+                    z = (M == -INFINITY) ? 0.0f : z * expf((m - M) * inv_t) + z2 * expf((m2 - M) * inv_t);
+                    m = M;
                 }
-                j = guard;
+                if (lane == 0) { scratch_m[0] = m; scratch_z[0] = z; }
             }
-            int len = s_len;
+            __syncthreads();
+            m = scratch_m[0];
+            z = scratch_z[0];
+        }
+        // child j: q(x_j) and its uniform, one thread each
+        const int nk = s_nkids;
+        if (threadIdx.x < nk) {
+            const int j = threadIdx.x;
+            const int x = s_kid_tok[j];
+            float q = 0.0f;
+            if (x >= 0 && x < V) q = expf((row[x] - m) * inv_t) / z;
+            else report(dev_status, DDT_DEV_BAD_TOKEN);
+            const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(u),
+                                                     static_cast<uint32_t>(j), off_lo), k0, k1);
+            s_q[j] = q;
+            s_u[j] = uniform_exact(w.x);
+        }
+        __syncthreads();
+        // children in rank order: accept child j when u_j * R < q(x_j)
+        if (threadIdx.x == 0) {
+            int match = -1;
+            double R = 1.0;
+            for (int j = 0; j < nk; ++j) {
+                if (s_u[j] * R < static_cast<double>(s_q[j])) { match = s_kid_node[j]; break; }
+                R -= static_cast<double>(s_q[j]);
+            }
+            const int len = s_len;
             if (match != -1 && len >= D) { report(dev_status, DDT_DEV_BAD_TREE); match = -1; }
             if (match != -1) {
-                toks[len] = token[tb + match];
+                toks[len] = tr.tok[match];
                 nodes[len + 1] = match;
                 s_len = len + 1;
             }
-            s_nkids = j;
             s_next = match;
         }
         __syncthreads();
         const int nxt = s_next;
         if (nxt != -1) { u = nxt; continue; }
         // bonus: Gumbel-max over tokens that are not children of u
-        const int nk = s_nkids;
         unsigned long long best = 0ull;
         const int groups = (V + 3) >> 2;
 #pragma unroll 4

@@ -8,41 +8,132 @@
 // Context section (top-k cap per node) and Hypothesis 3 (position =
 // ctx_len + depth).
 //
-// GPU design: one warp (one CTA) per request. The request's per-depth top-k is
-// staged in shared memory first, so the serial pop loop never waits on global
-// memory. The frontier (the heap's contents) lives in shared memory as a flat
-// array of at most budget+1 live entries; each pop is a warp-wide argmax over
-// (score desc, push sequence asc), which is the heap's total order, so the pop
-// sequence is the heap's exactly. Removal moves the last entry into the hole.
-// Scores are fp64 sums in path order, as in the definition.
+// GPU design: one warp (one CTA) per request, with the request's top-k staged
+// in shared memory. The heap is a warp-wide sorted list held in registers
+// (entry p in slot p / 32 of lane p % 32), ordered by a 64-bit integer key
+// that preserves the order of the fp64 score, newest last among equal keys.
+// That is the heap's total order (score descending, earlier push first), so a
+// pop takes entry 0 and an insert lands after every entry with a key >= its
+// own: one ballot and one shift. Only lane 0 touches fp64 (two adds per pop,
+// in path order, as in the definition). Masks, positions and child links are
+// then computed with every lane working on its own nodes.
 #include "common.cuh"
 
 namespace ddt {
 
 constexpr int kMaxN = DDT_MAX_NODES;          // 128
 constexpr int kMaxW = (kMaxN + 31) / 32;      // 4
-constexpr int kMaxFrontier = kMaxN;           // live entries <= 1 + budget <= 128
+constexpr int kSlots = kMaxN / 32;            // live heap entries <= 1 + budget <= 128
 
 struct BuildSmem {
-    double f_score[kMaxFrontier];
-    int f_seq[kMaxFrontier];
-    int f_code[kMaxFrontier];   // depth << 16 | rank << 8 | parent
     double n_score[kMaxN];
     int n_parent[kMaxN];
     int n_depth[kMaxN];
     int n_rank[kMaxN];
     int n_token[kMaxN];
-    int n_first[kMaxN];
-    int n_next[kMaxN];
-    int n_last[kMaxN];
-    uint32_t n_vis[kMaxN][kMaxW];
 };
 
-DDT_DEVINL double canon_score(double s) { return s != s ? -INFINITY : s; }
+// order-preserving key of a double (NaN ranks as -inf); 0 is below every key
+DDT_DEVINL unsigned long long score_key(double s) {
+    if (s != s) s = -INFINITY;
+    const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(s));
+    return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+DDT_DEVINL double key_score(unsigned long long k) {
+    const unsigned long long b = (k >> 63) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
+    return __longlong_as_double(static_cast<long long>(b));
+}
 
-// true if entry (s, q) comes before (bs, bq) in pop order
-DDT_DEVINL bool pops_before(double s, int q, double bs, int bq) {
-    return s > bs || (s == bs && q < bq);
+template <int SLOTS>
+struct WarpHeap {
+    unsigned long long key[SLOTS];
+    uint32_t code[SLOTS];   // depth << 16 | rank << 8 | parent
+
+    DDT_DEVINL void clear() {
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) { key[s] = 0ull; code[s] = 0u; }
+    }
+    // remove entry 0 (every other entry moves one place forward)
+    DDT_DEVINL void pop_front(int lane) {
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            unsigned long long k = __shfl_down_sync(0xffffffffu, key[s], 1);
+            uint32_t c = __shfl_down_sync(0xffffffffu, code[s], 1);
+            const unsigned long long kn = s + 1 < SLOTS ? __shfl_sync(0xffffffffu, key[(s + 1) % SLOTS], 0) : 0ull;
+            const uint32_t cn = s + 1 < SLOTS ? __shfl_sync(0xffffffffu, code[(s + 1) % SLOTS], 0) : 0u;
+            if (lane == 31) { k = kn; c = cn; }
+            key[s] = k;
+            code[s] = c;
+        }
+    }
+    // insert after every entry whose key is >= k (stable: later pushes go last)
+    DDT_DEVINL void insert(unsigned long long k, uint32_t c, int lane) {
+        int pos = 0;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) pos += __popc(__ballot_sync(0xffffffffu, key[s] >= k));
+        unsigned long long carry_k = 0ull;
+        uint32_t carry_c = 0u;
+#pragma unroll
+        for (int s = 0; s < SLOTS; ++s) {
+            const unsigned long long up_k = __shfl_up_sync(0xffffffffu, key[s], 1);
+            const uint32_t up_c = __shfl_up_sync(0xffffffffu, code[s], 1);
+            const unsigned long long last_k = __shfl_sync(0xffffffffu, key[s], 31);
+            const uint32_t last_c = __shfl_sync(0xffffffffu, code[s], 31);
+            const int p = s * 32 + lane;
+            const unsigned long long prev_k = lane == 0 ? carry_k : up_k;
+            const uint32_t prev_c = lane == 0 ? carry_c : up_c;
+            if (p == pos) { key[s] = k; code[s] = c; }
+            else if (p > pos) { key[s] = prev_k; code[s] = prev_c; }
+            carry_k = last_k;
+            carry_c = last_c;
+        }
+    }
+};
+
+template <int SLOTS>
+DDT_DEVINL int build_pops(BuildSmem& s, const float* lp, const int32_t* tk, int D, int K, int budget,
+                          int lane) {
+    WarpHeap<SLOTS> h;
+    h.clear();
+    int count = 0, live = 0;
+    if (budget >= 1) {
+        h.insert(score_key(0.0 + static_cast<double>(lp[0])), (1u << 16) | (0u << 8) | 0u, lane);
+        live = 1;
+    }
+    while (count < budget && live > 0) {
+        const unsigned long long bk = __shfl_sync(0xffffffffu, h.key[0], 0);
+        const uint32_t code = __shfl_sync(0xffffffffu, h.code[0], 0);
+        h.pop_front(lane);
+        --live;
+        const int d = static_cast<int>(code >> 16), r = static_cast<int>((code >> 8) & 0xffu),
+                  p = static_cast<int>(code & 0xffu);
+        ++count;
+        const int i = count;
+        double cs = 0.0, ss = 0.0;
+        if (lane == 0) {
+            const double sc = key_score(bk);
+            s.n_score[i] = sc;
+            s.n_parent[i] = p;
+            s.n_depth[i] = d;
+            s.n_rank[i] = r;
+            s.n_token[i] = tk[(d - 1) * K + r];
+            if (d < D) cs = sc + static_cast<double>(lp[d * K]);                 // best child
+            if (r + 1 < K) ss = s.n_score[p] + static_cast<double>(lp[(d - 1) * K + r + 1]);  // next sibling
+        }
+        const unsigned long long ck = __shfl_sync(0xffffffffu, score_key(cs), 0);
+        const unsigned long long sk = __shfl_sync(0xffffffffu, score_key(ss), 0);
+        if (d < D) {   // the child is pushed before the sibling
+            h.insert(ck, (static_cast<uint32_t>(d + 1) << 16) | (0u << 8) | static_cast<uint32_t>(i), lane);
+            ++live;
+        }
+        if (r + 1 < K) {
+            h.insert(sk, (static_cast<uint32_t>(d) << 16) | (static_cast<uint32_t>(r + 1) << 8) |
+                             static_cast<uint32_t>(p), lane);
+            ++live;
+        }
+        __syncwarp();
+    }
+    return count;
 }
 
 __global__ void __launch_bounds__(32)
@@ -65,11 +156,10 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
         const float* glp = topk_logp + static_cast<size_t>(b) * D * K;
         const int32_t* gtk = topk_tok + static_cast<size_t>(b) * D * K;
         for (int x = lane; x < D * K; x += 32) { lp[x] = glp[x]; tk[x] = gtk[x]; }
-        __syncwarp();
     }
     const int N = budget + 1;
     const int W = (N + 31) >> 5;
-
+    const int L = ctx_len[b];
     if (lane == 0) {
         s.n_score[0] = 0.0;
         s.n_parent[0] = -1;
@@ -77,109 +167,41 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
         s.n_rank[0] = 0;
         s.n_token[0] = root_tok[b];
     }
-    // warp-uniform bookkeeping (every lane keeps the same copy)
-    int fsize = 0, seqc = 0, count = 0;
-    if (budget >= 1) {
-        if (lane == 0) {
-            s.f_score[0] = canon_score(0.0 + static_cast<double>(lp[0]));
-            s.f_seq[0] = 0;
-            s.f_code[0] = (1 << 16) | (0 << 8) | 0;
-        }
-        fsize = 1;
-        seqc = 1;
-    }
     __syncwarp();
 
-    while (count < budget && fsize > 0) {
-        double bs = -INFINITY;
-        int bq = 0x7fffffff, bi = -1;
-        for (int e = lane; e < fsize; e += 32) {
-            const double sc = s.f_score[e];
-            const int q = s.f_seq[e];
-            if (bi < 0 || pops_before(sc, q, bs, bq)) { bs = sc; bq = q; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const double os = __shfl_xor_sync(0xffffffffu, bs, o);
-            const int oq = __shfl_xor_sync(0xffffffffu, bq, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi >= 0 && (bi < 0 || pops_before(os, oq, bs, bq))) { bs = os; bq = oq; bi = oi; }
-        }
-        const int code = s.f_code[bi];
-        const int d = code >> 16, r = (code >> 8) & 0xff, p = code & 0xff;
-        ++count;
-        const int i = count;
-        const bool push_child = d < D;
-        const bool push_sib = r + 1 < K;
-        __syncwarp();
-        if (lane == 0) {
-            --fsize;
-            s.f_score[bi] = s.f_score[fsize];
-            s.f_seq[bi] = s.f_seq[fsize];
-            s.f_code[bi] = s.f_code[fsize];
-            s.n_score[i] = bs;
-            s.n_parent[i] = p;
-            s.n_depth[i] = d;
-            s.n_rank[i] = r;
-            s.n_token[i] = tk[(d - 1) * K + r];
-            int e = fsize, q = seqc;
-            if (push_child) {   // best child: rank 0 of depth d+1
-                s.f_score[e] = canon_score(bs + static_cast<double>(lp[d * K]));
-                s.f_seq[e] = q++;
-                s.f_code[e] = ((d + 1) << 16) | (0 << 8) | i;
-                ++e;
-            }
-            if (push_sib) {     // next sibling: rank r+1 under the same parent
-                s.f_score[e] = canon_score(s.n_score[p] + static_cast<double>(lp[(d - 1) * K + r + 1]));
-                s.f_seq[e] = q++;
-                s.f_code[e] = (d << 16) | ((r + 1) << 8) | p;
-            }
-        } else {
-            --fsize;
-        }
-        fsize += static_cast<int>(push_child) + static_cast<int>(push_sib);
-        seqc += static_cast<int>(push_child) + static_cast<int>(push_sib);
-        __syncwarp();
-    }
+    int count;
+    if (N <= 32) count = build_pops<1>(s, lp, tk, D, K, budget, lane);
+    else if (N <= 64) count = build_pops<2>(s, lp, tk, D, K, budget, lane);
+    else count = build_pops<4>(s, lp, tk, D, K, budget, lane);
     const int n = count + 1;
-
-    // children as first-child / next-sibling links (index order = rank order)
-    for (int i = lane; i < n; i += 32) { s.n_first[i] = -1; s.n_next[i] = -1; s.n_last[i] = -1; }
     __syncwarp();
-    if (lane == 0) {
-        for (int i = 1; i < n; ++i) {
-            const int p = s.n_parent[i];
-            if (s.n_last[p] < 0) s.n_first[p] = i; else s.n_next[s.n_last[p]] = i;
-            s.n_last[p] = i;
-        }
-    }
-    // ancestor-or-self bitmask: vis[i] = vis[parent[i]] | bit(i), parents first
-    for (int i = 0; i < n; ++i) {
-        if (lane < W) {
-            uint32_t v = (i == 0) ? 0u : s.n_vis[s.n_parent[i]][lane];
-            if (lane == (i >> 5)) v |= 1u << (i & 31);
-            s.n_vis[i][lane] = v;
-        }
-        __syncwarp();
-    }
 
-    const int L = ctx_len[b];
     if (L < 0 && lane == 0) report(dev_status, DDT_DEV_BAD_CTX);
     const size_t base = static_cast<size_t>(b) * N;
     for (int i = lane; i < N; i += 32) {
         const bool real = i < n;
+        int fc = -1, ns = -1;
+        uint32_t vw[kMaxW] = {0u, 0u, 0u, 0u};
+        if (real) {
+            // children in index order = rank order: first child, next sibling
+            for (int c = i + 1; c < n; ++c)
+                if (s.n_parent[c] == i) { fc = c; break; }
+            const int pi = s.n_parent[i];
+            if (pi >= 0)
+                for (int c = i + 1; c < n; ++c)
+                    if (s.n_parent[c] == pi) { ns = c; break; }
+            // ancestor-or-self bits
+            for (int a = i; a >= 0; a = s.n_parent[a]) vw[a >> 5] |= 1u << (a & 31);
+        }
         parent[base + i] = real ? s.n_parent[i] : -1;
         depth[base + i] = real ? s.n_depth[i] : -1;
         token[base + i] = real ? s.n_token[i] : -1;
         rank[base + i] = real ? s.n_rank[i] : -1;
         pos[base + i] = real ? L + s.n_depth[i] : -1;
         score[base + i] = real ? s.n_score[i] : -INFINITY;
-        first_child[base + i] = real ? s.n_first[i] : -1;
-        next_sibling[base + i] = real ? s.n_next[i] : -1;
-    }
-    for (int x = lane; x < N * W; x += 32) {
-        const int i = x / W, w = x % W;
-        vis[base * W + x] = i < n ? s.n_vis[i][w] : 0u;
+        first_child[base + i] = fc;
+        next_sibling[base + i] = ns;
+        for (int w = 0; w < W; ++w) vis[(base + i) * W + w] = vw[w];
     }
     if (lane == 0) n_nodes_out[b] = n;
 }
