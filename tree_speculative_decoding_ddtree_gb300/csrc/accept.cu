@@ -8,15 +8,56 @@
 // Architecture of Speculative Verification: Implementing Temperature-Aware
 // Tree Sampling for DDTree", Path B (lazy softmax of the visited nodes only).
 //
-// One CTA per request walks the tree; only the logits rows of visited nodes
-// are read, each streamed once per pass with 16-byte loads, eight in flight
-// per thread so a row costs about one memory round trip.
+// One cluster of kCluster CTAs per request walks the tree. Only the logits
+// rows of visited nodes are read. Every pass over a row (argmax; running max
+// and softmax denominator; the Gumbel-max bonus) is split over the cluster:
+// CTA r streams slice r of the vocabulary with 16-byte loads, reduces it in
+// the block, and publishes one partial in its shared memory; after a cluster
+// barrier every CTA reads the kCluster partials through distributed shared
+// memory and combines them in rank order, so all CTAs hold the same result
+// and take the same step. The walk itself (child match, rejection tests) is
+// done by every CTA on identical values; CTA 0 writes the outputs. Per level
+// this costs one row slice (a memory round trip) and one cluster barrier,
+// instead of streaming the whole row through one SM.
 #include "common.cuh"
 
 namespace ddt {
 
-constexpr int kAcceptThreads = 1024;
+constexpr int kCluster = 8;               // CTAs per request (portable cluster size)
+constexpr int kWalkThreads = 512;
 constexpr int kMaxKids = DDT_MAX_TOPK;
+
+// ---------------------------------------------------------------------------
+// cluster helpers
+// ---------------------------------------------------------------------------
+DDT_DEVINL uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// every thread of every CTA of the cluster; orders shared-memory writes before
+// the barrier with reads after it, cluster-wide
+DDT_DEVINL void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// shared::cluster address of the same variable in CTA `rank`
+DDT_DEVINL uint32_t cluster_addr(const void* p, uint32_t rank) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+DDT_DEVINL unsigned long long ld_cluster_u64(uint32_t addr) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];\n" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+DDT_DEVINL float2 ld_cluster_f32x2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
 
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., SC'11): two multiply-xor lanes per round,
@@ -48,7 +89,7 @@ DDT_DEVINL double uniform_exact(uint32_t w) {
     return (static_cast<double>(w >> 8) + 0.5) * 0x1p-24;
 }
 
-// block-wide reductions over kAcceptThreads threads; every thread gets the result
+// block-wide reductions over kWalkThreads threads; every thread gets the result
 template <typename T, typename Op>
 DDT_DEVINL T block_reduce(T v, T* scratch, Op op, T identity) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -58,7 +99,7 @@ DDT_DEVINL T block_reduce(T v, T* scratch, Op op, T identity) {
     if (lane == 0) scratch[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        T x = lane < kAcceptThreads / 32 ? scratch[lane] : identity;
+        T x = lane < kWalkThreads / 32 ? scratch[lane] : identity;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) x = op(x, __shfl_xor_sync(0xffffffffu, x, o));
         if (lane == 0) scratch[0] = x;
@@ -68,17 +109,28 @@ DDT_DEVINL T block_reduce(T v, T* scratch, Op op, T identity) {
 }
 
 struct MaxU64 { DDT_DEVINL unsigned long long operator()(unsigned long long a, unsigned long long b) const { return a > b ? a : b; } };
-struct MaxF { DDT_DEVINL float operator()(float a, float b) const { return fmaxf(a, b); } };
-struct SumF { DDT_DEVINL float operator()(float a, float b) const { return a + b; } };
 
-// argmax of one row (largest value, lowest index, NaN lowest)
-DDT_DEVINL uint32_t row_argmax(const float* __restrict__ row, int V, bool vec4,
-                               unsigned long long* scratch) {
+// This CTA's slice of a row: float4 groups [g0, g1) when the row is read as
+// float4, else elements [g0, g1).
+struct Slice {
+    int g0, g1;
+};
+DDT_DEVINL Slice row_slice(int V, bool vec4, uint32_t rank) {
+    const int n = vec4 ? (V >> 2) : V;
+    Slice s;
+    s.g0 = static_cast<int>((static_cast<long long>(n) * rank) / kCluster);
+    s.g1 = static_cast<int>((static_cast<long long>(n) * (rank + 1)) / kCluster);
+    return s;
+}
+
+// argmax of this CTA's slice (largest value, lowest index, NaN lowest), packed
+DDT_DEVINL unsigned long long slice_argmax(const float* __restrict__ row, bool vec4, Slice sl,
+                                           unsigned long long* scratch) {
     unsigned long long best = 0ull;
     if (vec4) {
         const float4* r4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 8
-        for (int x = threadIdx.x; x < (V >> 2); x += kAcceptThreads) {
+#pragma unroll 4
+        for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads) {
             const float4 f = __ldg(r4 + x);
             const uint32_t v = static_cast<uint32_t>(x) << 2;
             unsigned long long p0 = argmax_pack(float_order_key(f.x), v);
@@ -91,13 +143,23 @@ DDT_DEVINL uint32_t row_argmax(const float* __restrict__ row, int V, bool vec4,
             best = best > p0 ? best : p0;
         }
     } else {
-        for (int v = threadIdx.x; v < V; v += kAcceptThreads) {
+        for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads) {
             const unsigned long long p = argmax_pack(float_order_key(__ldg(row + v)), v);
             best = best > p ? best : p;
         }
     }
-    best = block_reduce(best, scratch, MaxU64(), 0ull);
-    return argmax_unpack_idx(best);
+    return block_reduce(best, scratch, MaxU64(), 0ull);
+}
+
+// max over the cluster's partials (slot `part` in every CTA)
+DDT_DEVINL unsigned long long cluster_max_u64(const unsigned long long* part) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) {
+        const unsigned long long v = ld_cluster_u64(cluster_addr(part, r));
+        best = best > v ? best : v;
+    }
+    return best;
 }
 
 struct WalkOut {
@@ -117,53 +179,70 @@ struct TreeRows {
 
 DDT_DEVINL void stage_tree(TreeRows& t, const int32_t* token, const int32_t* first_child,
                            const int32_t* next_sibling, size_t tb, int N) {
-    for (int i = threadIdx.x; i < N; i += kAcceptThreads) {
+    for (int i = threadIdx.x; i < N; i += kWalkThreads) {
         t.tok[i] = token[tb + i];
         t.fc[i] = first_child[tb + i];
         t.ns[i] = next_sibling[tb + i];
     }
 }
 
-__global__ void __launch_bounds__(kAcceptThreads)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWalkThreads)
 accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
                      const int32_t* __restrict__ token, const int32_t* __restrict__ first_child,
                      const int32_t* __restrict__ next_sibling, const int32_t* __restrict__ n_nodes,
                      int N, int D, WalkOut o, int32_t* dev_status) {
     __shared__ unsigned long long scratch[32];
+    __shared__ unsigned long long part[2];      // this CTA's partial argmax, by level parity
     __shared__ TreeRows tr;
     __shared__ int s_next;
     __shared__ int s_len;
-    const int b = blockIdx.x;
+    const uint32_t rank = cluster_rank();
+    const bool writer = rank == 0;
+    const int b = static_cast<int>(blockIdx.x) / kCluster;
     const size_t tb = static_cast<size_t>(b) * N;
+    const Slice sl = row_slice(V, vec4, rank);
     int32_t* toks = o.out_tokens + static_cast<size_t>(b) * (D + 1);
     int32_t* nodes = o.out_nodes + static_cast<size_t>(b) * (D + 1);
-    for (int k = threadIdx.x; k <= D; k += kAcceptThreads) { toks[k] = -1; nodes[k] = -1; }
+    if (writer)
+        for (int k = threadIdx.x; k <= D; k += kWalkThreads) { toks[k] = -1; nodes[k] = -1; }
     stage_tree(tr, token, first_child, next_sibling, tb, N);
     int nn = n_nodes[b];
     if (nn < 1 || nn > N) {
-        if (threadIdx.x == 0) report(dev_status, DDT_DEV_BAD_TREE);
+        if (threadIdx.x == 0 && writer) report(dev_status, DDT_DEV_BAD_TREE);
         nn = nn < 1 ? 1 : N;
     }
     if (threadIdx.x == 0) s_len = 0;
     __syncthreads();
-    if (threadIdx.x == 0) nodes[0] = 0;
+    if (threadIdx.x == 0 && writer) nodes[0] = 0;
     int u = 0;
-    while (true) {
-        const uint32_t a = row_argmax(logits + (tb + u) * static_cast<size_t>(V), V, vec4, scratch);
+    for (int level = 0;; ++level) {
+        const unsigned long long mine = slice_argmax(logits + (tb + u) * static_cast<size_t>(V), vec4, sl, scratch);
+        if (threadIdx.x == 0) part[level & 1] = mine;
+        cluster_barrier();
         if (threadIdx.x == 0) {
+            // the same partials in the same order in every CTA: the same argmax
+            const uint32_t a = argmax_unpack_idx(cluster_max_u64(&part[level & 1]));
             int match = -1, c = tr.fc[u], guard = 0;
             while (c != -1) {
-                if (c < 1 || c >= nn || ++guard > kMaxKids) { report(dev_status, DDT_DEV_BAD_TREE); break; }
+                if (c < 1 || c >= nn || ++guard > kMaxKids) {
+                    if (writer) report(dev_status, DDT_DEV_BAD_TREE);
+                    break;
+                }
                 if (tr.tok[c] == static_cast<int32_t>(a)) { match = c; break; }
                 c = tr.ns[c];
             }
             const int len = s_len;
-            if (match != -1 && len >= D) { report(dev_status, DDT_DEV_BAD_TREE); match = -1; }
+            if (match != -1 && len >= D) {
+                if (writer) report(dev_status, DDT_DEV_BAD_TREE);
+                match = -1;
+            }
             if (match != -1) {
-                toks[len] = tr.tok[match];
-                nodes[len + 1] = match;
+                if (writer) {
+                    toks[len] = tr.tok[match];
+                    nodes[len + 1] = match;
+                }
                 s_len = len + 1;
-            } else {
+            } else if (writer) {
                 toks[len] = static_cast<int32_t>(a);
                 o.bonus[b] = static_cast<int32_t>(a);
                 o.accept_len[b] = len;
@@ -174,14 +253,23 @@ accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
         u = s_next;
         if (u == -1) break;
     }
+    cluster_barrier();   // peers may still be reading this CTA's partials
 }
 
-// online (max, sum of exp((x - max) / T)) pair, merged in a block reduction
+// online (max, sum of exp((x - max) / T)) pair
 struct MaxSum {
     float m, z;
 };
 
-__global__ void __launch_bounds__(kAcceptThreads)
+DDT_DEVINL MaxSum merge_ms(MaxSum a, MaxSum b, float inv_t) {
+    const float M = fmaxf(a.m, b.m);
+    MaxSum r;
+    r.m = M;
+    r.z = (M == -INFINITY) ? 0.0f : a.z * expf((a.m - M) * inv_t) + b.z * expf((b.m - M) * inv_t);
+    return r;
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWalkThreads)
 accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
                      const int32_t* __restrict__ token, const int32_t* __restrict__ first_child,
                      const int32_t* __restrict__ next_sibling, const int32_t* __restrict__ n_nodes,
@@ -191,29 +279,37 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     __shared__ unsigned long long scratch_u[32];
     __shared__ float scratch_m[32];
     __shared__ float scratch_z[32];
+    __shared__ float2 part_ms[2];               // this CTA's partial (max, sum), by level parity
+    __shared__ unsigned long long part_g;       // this CTA's partial Gumbel-max (bonus)
     __shared__ TreeRows tr;
     __shared__ int s_kid_tok[kMaxKids];
     __shared__ int s_kid_node[kMaxKids];
+    __shared__ float s_kid_logit[kMaxKids];
     __shared__ float s_q[kMaxKids];
     __shared__ double s_u[kMaxKids];
+    __shared__ float s_m, s_z;
     __shared__ int s_nkids;
     __shared__ int s_next;
     __shared__ int s_len;
-    const int b = blockIdx.x;
+    const uint32_t rank = cluster_rank();
+    const bool writer = rank == 0;
+    const int b = static_cast<int>(blockIdx.x) / kCluster;
     const size_t tb = static_cast<size_t>(b) * N;
+    const Slice sl = row_slice(V, vec4, rank);
     int32_t* toks = o.out_tokens + static_cast<size_t>(b) * (D + 1);
     int32_t* nodes = o.out_nodes + static_cast<size_t>(b) * (D + 1);
-    for (int k = threadIdx.x; k <= D; k += kAcceptThreads) { toks[k] = -1; nodes[k] = -1; }
+    if (writer)
+        for (int k = threadIdx.x; k <= D; k += kWalkThreads) { toks[k] = -1; nodes[k] = -1; }
     stage_tree(tr, token, first_child, next_sibling, tb, N);
     int nn = n_nodes[b];
     if (nn < 1 || nn > N) {
-        if (threadIdx.x == 0) report(dev_status, DDT_DEV_BAD_TREE);
+        if (threadIdx.x == 0 && writer) report(dev_status, DDT_DEV_BAD_TREE);
         nn = nn < 1 ? 1 : N;
     }
     const float T = temperature[b];
     __syncthreads();
-    if (!(T > 0.0f) || !isfinite(T)) {
-        if (threadIdx.x == 0) {
+    if (!(T > 0.0f) || !isfinite(T)) {   // the same decision in every CTA of the cluster
+        if (threadIdx.x == 0 && writer) {
             report(dev_status, DDT_DEV_BAD_TEMPERATURE);
             o.accept_len[b] = 0;
             o.bonus[b] = -1;
@@ -225,15 +321,21 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     const uint32_t k0 = static_cast<uint32_t>(sd), k1 = static_cast<uint32_t>(sd >> 32);
     const uint32_t off_lo = static_cast<uint32_t>(offset);
     const uint32_t off_hi8 = static_cast<uint32_t>(offset >> 32) << 8;
-    if (threadIdx.x == 0) { s_len = 0; nodes[0] = 0; }
+    if (threadIdx.x == 0) {
+        s_len = 0;
+        if (writer) nodes[0] = 0;
+    }
     int u = 0;
-    while (true) {
+    for (int level = 0;; ++level) {
         const float* row = logits + (tb + u) * static_cast<size_t>(V);
         // the node's children, in rank order (thread 0, from shared memory)
         if (threadIdx.x == 0) {
             int c = tr.fc[u], j = 0;
             while (c != -1) {
-                if (c < 1 || c >= nn || j >= kMaxKids) { report(dev_status, DDT_DEV_BAD_TREE); break; }
+                if (c < 1 || c >= nn || j >= kMaxKids) {
+                    if (writer) report(dev_status, DDT_DEV_BAD_TREE);
+                    break;
+                }
                 s_kid_node[j] = c;
                 s_kid_tok[j] = tr.tok[c];
                 ++j;
@@ -241,64 +343,74 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
             }
             s_nkids = j;
         }
-        // one pass: running max and softmax denominator of logits / T
-        float m = -INFINITY, z = 0.0f;
+        __syncthreads();
+        const int nk = s_nkids;
+        // the children's logits are fetched while the slice streams
+        if (threadIdx.x < nk) {
+            const int x = s_kid_tok[threadIdx.x];
+            s_kid_logit[threadIdx.x] = (x >= 0 && x < V) ? __ldg(row + x) : 0.0f;
+        }
+        // this CTA's slice: running max and softmax denominator of logits / T
+        MaxSum ms{-INFINITY, 0.0f};
         auto add = [&](float x) {
-            if (x > m) {
-                z = z * expf((m - x) * inv_t) + 1.0f;
-                m = x;
+            if (x > ms.m) {
+                ms.z = ms.z * expf((ms.m - x) * inv_t) + 1.0f;
+                ms.m = x;
             } else {
-                z += expf((x - m) * inv_t);
+                ms.z += expf((x - ms.m) * inv_t);
             }
         };
         if (vec4) {
             const float4* r4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 8
-            for (int x = threadIdx.x; x < (V >> 2); x += kAcceptThreads) {
+#pragma unroll 4
+            for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads) {
                 const float4 f = __ldg(r4 + x);
                 add(f.x); add(f.y); add(f.z); add(f.w);
             }
         } else {
-            for (int v = threadIdx.x; v < V; v += kAcceptThreads) add(__ldg(row + v));
+            for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads) add(__ldg(row + v));
         }
         {
             const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
-                const float M = fmaxf(m, m2);
-                z = (M == -INFINITY) ? 0.0f : z * expf((m - M) * inv_t) + z2 * expf((m2 - M) * inv_t);
-                m = M;
+                MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
+                ms = merge_ms(ms, other, inv_t);
             }
             __syncthreads();
-            if (lane == 0) { scratch_m[warp] = m; scratch_z[warp] = z; }
+            if (lane == 0) { scratch_m[warp] = ms.m; scratch_z[warp] = ms.z; }
             __syncthreads();
             if (warp == 0) {
-                m = lane < kAcceptThreads / 32 ? scratch_m[lane] : -INFINITY;
-                z = lane < kAcceptThreads / 32 ? scratch_z[lane] : 0.0f;
+                ms.m = lane < kWalkThreads / 32 ? scratch_m[lane] : -INFINITY;
+                ms.z = lane < kWalkThreads / 32 ? scratch_z[lane] : 0.0f;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
-                    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                    const float z2 = __shfl_xor_sync(0xffffffffu, z, off);
-                    const float M = fmaxf(m, m2);
-                    z = (M == -INFINITY) ? 0.0f : z * expf((m - M) * inv_t) + z2 * expf((m2 - M) * inv_t);
-                    m = M;
+                    MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
+                    ms = merge_ms(ms, other, inv_t);
                 }
-                if (lane == 0) { scratch_m[0] = m; scratch_z[0] = z; }
+                if (lane == 0) part_ms[level & 1] = make_float2(ms.m, ms.z);
             }
-            __syncthreads();
-            m = scratch_m[0];
-            z = scratch_z[0];
         }
+        cluster_barrier();
+        if (threadIdx.x == 0) {
+            // the same partials merged in the same order in every CTA
+            MaxSum acc{-INFINITY, 0.0f};
+#pragma unroll
+            for (int r = 0; r < kCluster; ++r) {
+                const float2 pr = ld_cluster_f32x2(cluster_addr(&part_ms[level & 1], r));
+                acc = merge_ms(acc, MaxSum{pr.x, pr.y}, inv_t);
+            }
+            s_m = acc.m;
+            s_z = acc.z;
+        }
+        __syncthreads();
         // child j: q(x_j) and its uniform, one thread each
-        const int nk = s_nkids;
         if (threadIdx.x < nk) {
             const int j = threadIdx.x;
             const int x = s_kid_tok[j];
             float q = 0.0f;
-            if (x >= 0 && x < V) q = expf((row[x] - m) * inv_t) / z;
-            else report(dev_status, DDT_DEV_BAD_TOKEN);
+            if (x >= 0 && x < V) q = expf((s_kid_logit[j] - s_m) * inv_t) / s_z;
+            else if (writer) report(dev_status, DDT_DEV_BAD_TOKEN);
             const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(u),
                                                      static_cast<uint32_t>(j), off_lo), k0, k1);
             s_q[j] = q;
@@ -314,10 +426,15 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
                 R -= static_cast<double>(s_q[j]);
             }
             const int len = s_len;
-            if (match != -1 && len >= D) { report(dev_status, DDT_DEV_BAD_TREE); match = -1; }
+            if (match != -1 && len >= D) {
+                if (writer) report(dev_status, DDT_DEV_BAD_TREE);
+                match = -1;
+            }
             if (match != -1) {
-                toks[len] = tr.tok[match];
-                nodes[len + 1] = match;
+                if (writer) {
+                    toks[len] = tr.tok[match];
+                    nodes[len + 1] = match;
+                }
                 s_len = len + 1;
             }
             s_next = match;
@@ -325,11 +442,11 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         __syncthreads();
         const int nxt = s_next;
         if (nxt != -1) { u = nxt; continue; }
-        // bonus: Gumbel-max over tokens that are not children of u
+        // bonus: Gumbel-max over this CTA's slice, tokens that are not children of u
         unsigned long long best = 0ull;
-        const int groups = (V + 3) >> 2;
-#pragma unroll 4
-        for (int x = threadIdx.x; x < groups; x += kAcceptThreads) {
+        const int g0 = vec4 ? sl.g0 : (sl.g0 >> 2), g1 = vec4 ? sl.g1 : ((sl.g1 + 3) >> 2);
+#pragma unroll 2
+        for (int x = g0 + static_cast<int>(threadIdx.x); x < g1; x += kWalkThreads) {
             const uint4 w = philox4x32_10(make_uint4(1u | off_hi8, static_cast<uint32_t>(u),
                                                      static_cast<uint32_t>(x), off_lo), k0, k1);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -344,7 +461,8 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int v = 4 * x + e;
-                if (v >= V) break;
+                // element slices: this CTA owns [g0, g1) of the elements only
+                if (v >= V || (!vec4 && (v < sl.g0 || v >= sl.g1))) continue;
                 bool kid = false;
                 for (int k = 0; k < nk; ++k) kid |= (s_kid_tok[k] == v);
                 if (kid) continue;
@@ -355,15 +473,19 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
             }
         }
         best = block_reduce(best, scratch_u, MaxU64(), 0ull);
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0) part_g = best;
+        cluster_barrier();
+        if (threadIdx.x == 0 && writer) {
+            const unsigned long long all = cluster_max_u64(&part_g);
             const int len = s_len;
-            const int32_t a = best ? static_cast<int32_t>(argmax_unpack_idx(best)) : -1;
+            const int32_t a = all ? static_cast<int32_t>(argmax_unpack_idx(all)) : -1;
             toks[len] = a;
             o.bonus[b] = a;
             o.accept_len[b] = len;
         }
         break;
     }
+    cluster_barrier();   // peers may still be reading this CTA's partials
 }
 
 cudaError_t launch_accept_greedy(const float* logits, int V, const int32_t* token,
@@ -373,8 +495,8 @@ cudaError_t launch_accept_greedy(const float* logits, int V, const int32_t* toke
                                  int32_t* bonus, int32_t* dev_status, cudaStream_t stream) {
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
     WalkOut o{accept_len, out_tokens, out_nodes, bonus};
-    accept_greedy_kernel<<<B, kAcceptThreads, 0, stream>>>(logits, V, vec4, token, first_child,
-                                                           next_sibling, n_nodes, N, D, o, dev_status);
+    accept_greedy_kernel<<<B * kCluster, kWalkThreads, 0, stream>>>(logits, V, vec4, token, first_child,
+                                                                    next_sibling, n_nodes, N, D, o, dev_status);
     return cudaGetLastError();
 }
 
@@ -386,9 +508,9 @@ cudaError_t launch_accept_sample(const float* logits, int V, const int32_t* toke
                                  int32_t* bonus, int32_t* dev_status, cudaStream_t stream) {
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
     WalkOut o{accept_len, out_tokens, out_nodes, bonus};
-    accept_sample_kernel<<<B, kAcceptThreads, 0, stream>>>(logits, V, vec4, token, first_child,
-                                                           next_sibling, n_nodes, N, D, temperature,
-                                                           seed, offset, o, dev_status);
+    accept_sample_kernel<<<B * kCluster, kWalkThreads, 0, stream>>>(logits, V, vec4, token, first_child,
+                                                                    next_sibling, n_nodes, N, D, temperature,
+                                                                    seed, offset, o, dev_status);
     return cudaGetLastError();
 }
 
