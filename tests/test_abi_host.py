@@ -90,6 +90,10 @@ def attn_args(**kw):
     (dict(B=-1), -1), (dict(B=0, q=0), 0),
 ])
 def test_attn_rejects_bad_arguments(lib, kw, code):
+    if code == -6:
+        # the workspace cases rely on these sizes needing one: make sure, so that
+        # a call that is not refused can never launch on the placeholder pointers
+        assert lib.tree_verify_attn_workspace_size(2, 33, 64, 8, 128, 64 * 256) > 16
     assert lib.tree_verify_attn(*attn_args(**kw)) == code
 
 

@@ -65,14 +65,25 @@ def test_noalloc_matches_tree_verify_attn_twice():
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
-    w = S.config("deep")
+    # Hq/Hkv = 6 does not divide 128, so the warp-MMA kernel takes the call:
+    # 96 nodes x 6 heads = 576 rows (two row groups of 288) over up to 256k
+    # tokens of context need more split-KV scratch than the array holds. The
+    # need is checked with the library's own workspace_size first, and the
+    # entry point is called (with placeholder pointers) only when it exceeds
+    # the array: the call must then return DDT_ESCRATCH on the host, before
+    # anything is launched.
     lib = dd.load_library()
+    B, N, Hq, Hkv, Dh, page, max_pages = 2, 96, 48, 8, 128, 64, 4096
+    cap = lib.tree_verify_attn_noalloc_max_scratch
+    cap.restype = ctypes.c_size_t
+    need = lib.tree_verify_attn_workspace_size(B, N, Hq, Hkv, Dh, page * max_pages)
+    assert need > cap(), "these sizes no longer exceed the scratch array; pick larger ones"
     fn = lib.tree_verify_attn_noalloc
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     fn.restype = I
     fn.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P, I, I, I, I, I, F, P, P, P, P]
     fake = 4096
-    st = fn(fake, fake, fake, fake, fake, 64 * 512, 64, fake, 512, fake, fake, fake,
-            w.B, w.N, w.Hq, w.Hkv, w.Dh, 0.1, fake, 0, 0, 0)
+    st = fn(fake, fake, fake, fake, fake, 16 * max_pages, page, fake, max_pages, fake, fake, fake,
+            B, N, Hq, Hkv, Dh, 0.1, fake, 0, 0, 0)
     assert st == -7
     assert b"scratch" in lib.ddtree_status_string(-7)
