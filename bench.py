@@ -30,6 +30,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "tree-verify steps/s & attn HBM GB/s (% roofline), batch16 ctx8k budget32"
+# DRAM traffic of one attn_tc_kernel launch on the batched workload:
+# dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture (--set full,
+# one launch) of `bench.py --steps 5 --warmup 3 --no-cpu-baseline --e2e-steps 3`.
+# Taken on the current kernel; to be refreshed (or set to None) when it changes.
+ATTN_TC_TRAFFIC_BYTES = 533.478144e6 + 30.209280e6
 WORKLOAD_DESC = ("batched serving: 16 requests, ctx ~U[1024,16384] paged (page 64, shuffled), "
                  "Hq 64 / Hkv 8 / Dh 128 bf16, budget 32 (N=33), top-k 8, depth 8, vocab 32000")
 
@@ -489,7 +494,9 @@ def run_native(args):
                        "l2": "inputs larger than L2 (paged KV cache %.0f MB > 129 MB L2)"
                              % (h["kv"]["k_cache"].nbytes * 2 / 1e6)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None,
+                         "frac": achieved / hbm_peak,
+                         "traffic": ATTN_TC_TRAFFIC_BYTES if w.name == "batched" else None,
+                         "traffic_source": "ncu dram read+write of one attn_tc_kernel launch, batched workload",
                          "kernel": "tree_verify_attn (split-KV main + combine launches)",
                          "peak_source": f"{peak_src} hbm_gbs",
                          "algorithmic_bytes": abytes, "attn_us": attn_avg_ms * 1e3,
