@@ -1,9 +1,9 @@
 """Benchmark of the DDTree tree-verify step on GB300.
 
 One step = the whole hot path over one batch: ddtree_build -> tree_verify_attn
--> ddtree_accept_greedy -> ddtree_accept_sample (the sampled walk runs on the
+-> ddtree_accept_greedy and ddtree_accept_sample (the sampled walk runs on the
 same tree at T = 0.7, as a server would for the temperature requests of a
-batch). The default workload is the batched serving case: 16 requests with
+batch; the two walks are independent and run concurrently on two streams). The default workload is the batched serving case: 16 requests with
 contexts uniform in [1024, 16384] tokens (paged, page 64, shuffled pages),
 64 query / 8 KV heads, head dim 128, budget 32 (33 verify rows), top-k cap 8,
 depth 8, vocab 32000. Inputs are seeded synthetic data (ddtree_synth).
@@ -342,12 +342,20 @@ def run_native(args):
     so = {k: torch.empty_like(t) for k, t in go.items()}
     scale = 1.0 / math.sqrt(w.Dh)
 
+    walk_stream = torch.cuda.Stream(device)
+
     def step():
         dd.ddtree_build(topk_logp, topk_tok, root, ctx, w.budget, out=tree, dev_status=status)
         dd.tree_verify_attn(q, k_tree, v_tree, k_cache, v_cache, table, ctx, tree.vis, tree.n_nodes,
                             scale, out=out, workspace=workspace, dev_status=status)
+        # the two walks read the same tree and logits and write separate outputs:
+        # the sampled walk runs on a second stream, concurrently with the greedy one
+        cur = torch.cuda.current_stream()
+        walk_stream.wait_stream(cur)
         dd.ddtree_accept_greedy(logits, tree, w.D, out=go, dev_status=status)
-        dd.ddtree_accept_sample(logits, tree, w.D, temp, seed, 0, out=so, dev_status=status)
+        with torch.cuda.stream(walk_stream):
+            dd.ddtree_accept_sample(logits, tree, w.D, temp, seed, 0, out=so, dev_status=status)
+        cur.wait_stream(walk_stream)
 
     for _ in range(max(args.warmup, 3)):
         step()

@@ -298,7 +298,10 @@ attn_mma_kernel(AttnParams p) {
 }
 
 // Merge the chunk partials of every multi-chunk (request, KV head): one warp
-// per query row, each lane owning DH/32 contiguous features.
+// per query row. The lanes read the chunks' (max, sum) pairs in parallel for
+// the common max and the total; then each lane owns DH/32 contiguous features
+// and adds the chunks' vectors, weighted by the chunk's exp2(max - M), with
+// the weights handed round by shuffles so several chunk loads are in flight.
 template <int DH>
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(AttnParams p) {
@@ -316,22 +319,40 @@ attn_combine_kernel(AttnParams p) {
     const int G = p.G;
     const int i = r / G, h = kvh * G + r % G;
     const size_t slot0 = (static_cast<size_t>(b) * p.Hkv + kvh) * p.max_chunks;
+    const float2* ml = p.ws_ml + slot0 * p.R + r;            // chunk c at ml[c * R]
     float M = -INFINITY;
-    for (int c = 0; c < nchunks; ++c) M = fmaxf(M, p.ws_ml[(slot0 + c) * p.R + r].x);
+    for (int c = lane; c < nchunks; c += 32) M = fmaxf(M, ml[static_cast<size_t>(c) * p.R].x);
+    M = warp_max_f(M);
     const float m_use = (M == -INFINITY) ? 0.0f : M;
     constexpr int PER = DH / 32;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
-    float lsum = 0.0f;
-    for (int c = 0; c < nchunks; ++c) {
-        const float2 ml = p.ws_ml[(slot0 + c) * p.R + r];
-        const float w = exp2f(ml.x - m_use);
-        lsum += ml.y * w;
-        const float* src = p.ws_o + ((slot0 + c) * p.R + r) * DH + lane * PER;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] += src[e] * w;
+    float lpart = 0.0f;
+    const float* o_row = p.ws_o + (slot0 * p.R + r) * DH + lane * PER;
+    const size_t o_stride = static_cast<size_t>(p.R) * DH;   // one chunk
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+        float wl = 0.0f;
+        if (c0 + lane < nchunks) {
+            const float2 v = ml[static_cast<size_t>(c0 + lane) * p.R];
+            wl = exp2f(v.x - m_use);
+            lpart += v.y * wl;
+        }
+        const int cn = min(32, nchunks - c0);
+#pragma unroll 4
+        for (int k = 0; k < cn; ++k) {
+            const float w = __shfl_sync(0xffffffffu, wl, k);
+            const float* src = o_row + static_cast<size_t>(c0 + k) * o_stride;
+            if constexpr (PER == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(src);
+                acc[0] += v.x * w; acc[1] += v.y * w; acc[2] += v.z * w; acc[3] += v.w * w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(src);
+                acc[0] += v.x * w; acc[1] += v.y * w;
+            }
+        }
     }
+    const float lsum = warp_sum_f(lpart);
     const bool real = nn_ok && i < nn;
     const float inv = (real && lsum > 0.0f) ? 1.0f / lsum : 0.0f;
     bf16_t* dst = p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * DH + lane * PER;
