@@ -253,6 +253,51 @@ def test_attn_bad_page_and_ctx_flagged():
     check_attn(o[0, :, 2:4, :].astype(np.float64), ref, "bad-case request 0")
 
 
+def test_attn_tc_bad_requests_between_good_ones():
+    """Tensor-core path: requests with an invalid length or node count get zero
+    rows, lse -inf and the BAD_CTX bit; the requests around them are unaffected."""
+    w = S.Workload(name="badtc", B=5, D=4, V=50, K=4, budget=20, Hq=16, Hkv=2, Dh=128, ctx_lo=0,
+                   ctx_hi=3000, page_size=64, paged_shuffle=True, seed=9)
+    st = stage(w, logits=False, ctx=[300, 700, 0, 2999, 65])
+    ctx_bad = st.ctx.copy()
+    ctx_bad[1] = 10 ** 6                          # beyond the page table
+    tree = gpu_tree(st)
+    nn = tree.n_nodes.clone()
+    nn[3] = -1                                    # invalid node count
+    s = status()
+    lse = torch.empty((w.B, w.N, w.Hq), dtype=torch.float32, device="cuda")
+    out = dd.tree_verify_attn(dev(st.qkv["q"]), dev(st.qkv["k_tree"]), dev(st.qkv["v_tree"]),
+                              dev(st.kv["k_cache"]), dev(st.kv["v_cache"]), dev(st.table),
+                              dev(ctx_bad), tree.vis, nn, scale(w), lse=lse, dev_status=s)
+    torch.cuda.synchronize()
+    assert int(s.item()) == 2
+    o = out.float().cpu().numpy()
+    assert np.all(o[1] == 0) and np.all(o[3] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[[1, 3]]))
+    G = w.G
+    for b in (0, 2, 4):
+        for kvh in range(w.Hkv):
+            check_attn(o[b, :, kvh * G:(kvh + 1) * G, :].astype(np.float64), oracle_slice(st, b, kvh),
+                       f"request {b} kv {kvh}")
+
+
+def test_attn_tc_many_short_requests():
+    """Tensor-core path with 40 short requests (0..699 cached tokens, 264 rows:
+    two tensor-core tiles and 8 leftover rows), full oracle comparison."""
+    rng = np.random.default_rng(31)
+    ctx = rng.integers(0, 700, size=40).tolist()
+    w = S.Workload(name="short", B=40, D=6, V=300, K=6, budget=32, Hq=64, Hkv=8, Dh=128, ctx_lo=0,
+                   ctx_hi=max(ctx), page_size=64, paged_shuffle=True, seed=123)
+    st = stage(w, logits=False, ctx=ctx)
+    out, lse = run_attn(st, lse=True)
+    ref, ref_lse = oracle_full(st, want_lse=True)
+    check_attn(out.float().cpu().numpy().astype(np.float64), ref, "many short")
+    got_lse = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(fin, np.isfinite(got_lse))
+    assert np.abs(got_lse[fin] - ref_lse[fin]).max() < 2e-3
+
+
 def test_attn_repeatable():
     st = stage(S.config("tiny"), logits=False)
     a, _ = run_attn(st)

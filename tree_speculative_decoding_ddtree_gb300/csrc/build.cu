@@ -33,10 +33,11 @@ struct BuildSmem {
     int n_token[kMaxN];
 };
 
-// order-preserving key of a double (NaN ranks as -inf); 0 is below every key
+// order-preserving key of a double (NaN ranks as -inf); 0 is below every key.
+// Integer operations only: fp64 compares are slow on this GPU.
 DDT_DEVINL unsigned long long score_key(double s) {
-    if (s != s) s = -INFINITY;
-    const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(s));
+    unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(s));
+    if ((b & 0x7FFFFFFFFFFFFFFFull) > 0x7FF0000000000000ull) b = 0xFFF0000000000000ull;   // NaN -> -inf
     return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
 }
 DDT_DEVINL double key_score(unsigned long long k) {
@@ -90,14 +91,16 @@ struct WarpHeap {
     }
 };
 
+// lp: the request's top-k log-probs, already widened to fp64 (exactly), so
+// the loop's only fp64 instructions are the two independent score adds per pop
 template <int SLOTS>
-DDT_DEVINL int build_pops(BuildSmem& s, const float* lp, const int32_t* tk, int D, int K, int budget,
+DDT_DEVINL int build_pops(BuildSmem& s, const double* lp, const int32_t* tk, int D, int K, int budget,
                           int lane) {
     WarpHeap<SLOTS> h;
     h.clear();
     int count = 0, live = 0;
     if (budget >= 1) {
-        h.insert(score_key(0.0 + static_cast<double>(lp[0])), (1u << 16) | (0u << 8) | 0u, lane);
+        h.insert(score_key(0.0 + lp[0]), (1u << 16) | (0u << 8) | 0u, lane);
         live = 1;
     }
     while (count < budget && live > 0) {
@@ -117,8 +120,8 @@ DDT_DEVINL int build_pops(BuildSmem& s, const float* lp, const int32_t* tk, int 
             s.n_depth[i] = d;
             s.n_rank[i] = r;
             s.n_token[i] = tk[(d - 1) * K + r];
-            if (d < D) cs = sc + static_cast<double>(lp[d * K]);                 // best child
-            if (r + 1 < K) ss = s.n_score[p] + static_cast<double>(lp[(d - 1) * K + r + 1]);  // next sibling
+            if (d < D) cs = sc + lp[d * K];                                 // best child
+            if (r + 1 < K) ss = s.n_score[p] + lp[(d - 1) * K + r + 1];      // next sibling
         }
         const unsigned long long ck = __shfl_sync(0xffffffffu, score_key(cs), 0);
         const unsigned long long sk = __shfl_sync(0xffffffffu, score_key(ss), 0);
@@ -147,15 +150,15 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
                     uint32_t* __restrict__ vis, int32_t* __restrict__ n_nodes_out,
                     int32_t* dev_status) {
     __shared__ BuildSmem s;
-    extern __shared__ unsigned char dyn[];     // staged top-k: D*K floats then D*K ints
+    extern __shared__ __align__(16) unsigned char dyn[];   // staged top-k: D*K doubles then D*K ints
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x;
-    float* lp = reinterpret_cast<float*>(dyn);
-    int32_t* tk = reinterpret_cast<int32_t*>(dyn + sizeof(float) * D * K);
+    double* lp = reinterpret_cast<double*>(dyn);
+    int32_t* tk = reinterpret_cast<int32_t*>(dyn + sizeof(double) * D * K);
     {
         const float* glp = topk_logp + static_cast<size_t>(b) * D * K;
         const int32_t* gtk = topk_tok + static_cast<size_t>(b) * D * K;
-        for (int x = lane; x < D * K; x += 32) { lp[x] = glp[x]; tk[x] = gtk[x]; }
+        for (int x = lane; x < D * K; x += 32) { lp[x] = static_cast<double>(glp[x]); tk[x] = gtk[x]; }
     }
     const int N = budget + 1;
     const int W = (N + 31) >> 5;
@@ -212,7 +215,7 @@ cudaError_t launch_build(const float* topk_logp, const int32_t* topk_tok, const 
                          int32_t* pos, double* score, int32_t* first_child,
                          int32_t* next_sibling, uint32_t* vis, int32_t* n_nodes,
                          int32_t* dev_status, cudaStream_t stream) {
-    const size_t dyn = static_cast<size_t>(D) * K * 8;
+    const size_t dyn = static_cast<size_t>(D) * K * 12;
     ddtree_build_kernel<<<B, 32, dyn, stream>>>(
         topk_logp, topk_tok, root_tok, ctx_len, B, D, K, budget, parent, depth, token, rank,
         pos, score, first_child, next_sibling, vis, n_nodes, dev_status);
