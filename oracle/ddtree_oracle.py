@@ -56,9 +56,13 @@ def draft_topk(draft_logits: np.ndarray, K: int):
     with their log-probs. [Branch] §"Hypothesis 4": each depth's distribution
     is conditioned on the anchor only, so one row per depth serves every node.
 
-    Reading (pages silent): log-softmax in fp64 over the row, top-K by value
-    with ties going to the lower token id, then rounded to fp32; these fp32
-    arrays are what both the oracle and the CUDA path consume.
+    Reading (pages silent): top-K tokens by the value of the draft logit
+    (log-softmax subtracts one constant per row, so this is the log-prob
+    order; ranking on the logit itself keeps distinct logits distinct where
+    the fp64 subtraction would round them to one value), ties going to the
+    lower token id; their log-probs are computed in fp64 over the row, then
+    rounded to fp32. These fp32 arrays are what both the oracle and the CUDA
+    path consume.
 
     Returns ``(topk_logp fp32 [B,D,K], topk_tok int32 [B,D,K])``.
     """
@@ -76,7 +80,7 @@ def draft_topk(draft_logits: np.ndarray, K: int):
     ids = np.arange(V)
     for b in range(B):
         for d in range(D):
-            order = np.lexsort((ids, -logp[b, d]))[:K]
+            order = np.lexsort((ids, -x[b, d]))[:K]
             tok[b, d] = order
             val[b, d] = logp[b, d, order].astype(np.float32)
     return val, tok

@@ -44,6 +44,20 @@ def test_draft_topk_matches_torch_logsoftmax_topk():
     assert np.array_equal(lp, v.numpy().astype(np.float32))
 
 
+def test_draft_topk_ranks_by_logit_where_fp64_logprobs_merge():
+    # 1e-10 and the next fp32 value above it differ by ~6e-18, far below the
+    # fp64 spacing near the row's log-sum-exp (~30): their fp64 log-probs are
+    # equal, but the larger logit still ranks first
+    a = np.float32(1e-10)
+    b = np.nextafter(a, np.float32(1))
+    x = np.array([[[30.0, a, b, -5.0]]], dtype=np.float32)
+    lse = 30.0 + math.log(sum(math.exp(float(v) - 30.0) for v in x[0, 0]))
+    assert float(a) - lse == float(b) - lse
+    lp, tok = O.draft_topk(x, 3)
+    assert tok[0, 0].tolist() == [0, 2, 1]
+    assert lp[0, 0, 1] == lp[0, 0, 2] == np.float32(float(b) - lse)
+
+
 def test_draft_topk_tie_goes_to_lower_token():
     x = np.zeros((1, 1, 6), np.float32)
     x[0, 0, [4, 1, 3]] = 2.0
