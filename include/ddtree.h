@@ -2,8 +2,10 @@
  * ddtree.h - C ABI of the DDTree tree-verify step on one GB300 (sm_103a).
  *
  * The step has four calls, taken in this order for one speculative-decoding
- * step of a batch of B requests:
+ * step of a batch of B requests, after an optional fifth that prepares the
+ * first one's input on the device:
  *
+ *   ddtree_draft_topk     draft logits -> per-depth top-k tokens + log-probs
  *   ddtree_build          per-depth top-k  -> best-first tree, mask, positions
  *   tree_verify_attn      tree rows attend to their context (paged KV, read
  *                         once per request and KV head) plus visible tree rows
@@ -89,6 +91,33 @@ const char* ddtree_status_string(int status);
 /* Text of the last CUDA error seen by a call that returned DDT_ECUDA on this
  * host thread ("" if none). */
 const char* ddtree_last_error(void);
+
+/*
+ * ddtree_draft_topk - per-depth top-K of the draft, with log-probs.
+ *
+ * [Arch] Section 1 (The Five-Step Flow of DDTree), step 1: the draft runs once
+ * over the block and, at each depth position, its top-k tokens are kept with
+ * their log-probs. [Branch] Hypothesis 4: one distribution per depth, shared
+ * by every node of that depth. The output is exactly ddtree_build's input.
+ *
+ * Inputs
+ *   draft_logits  fp32 [B, D, V]  the draft's logits, depth d's row for the
+ *                                 tokens at depth d+1
+ * Outputs
+ *   topk_logp     fp32  [B, D, K] log-probs, descending along K
+ *   topk_tok      int32 [B, D, K] their token ids
+ * Ranking is by the logit (the same order as the log-prob), ties to the lower
+ * token id, NaN below every number (-0 equals +0). The log-prob is the logit
+ * minus the row's log-sum-exp, taken in fp64 from an fp32 exp-sum and rounded
+ * to fp32 (about 1e-5 absolute from the fp64 value at V = 131072). A row
+ * holding a NaN or +inf, or only -inf, has a NaN log-sum-exp: its K tokens
+ * are still ranked and its log-probs are NaN.
+ * 1 <= K <= min(32, V), 1 <= D <= 64, B * D < 2^31. Rows are read with 16-byte
+ * loads when V % 4 == 0 and draft_logits is 16-byte aligned, else 4-byte.
+ * No device errors.
+ */
+int ddtree_draft_topk(const float* draft_logits, int B, int D, int V, int K,
+                      float* topk_logp, int32_t* topk_tok, void* stream);
 
 /*
  * ddtree_build - best-first draft tree from the per-depth top-k.

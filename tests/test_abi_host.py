@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_four_calls():
     names = declared_functions()
-    for n in ("ddtree_build", "tree_verify_attn", "ddtree_accept_greedy", "ddtree_accept_sample"):
+    for n in ("ddtree_draft_topk", "ddtree_build", "tree_verify_attn", "ddtree_accept_greedy", "ddtree_accept_sample"):
         assert n in names
 
 
@@ -70,6 +70,25 @@ def test_build_rejects_null_pointers(lib, null):
 
 def test_build_empty_batch_is_a_noop(lib):
     assert lib.ddtree_build(*build_args(B=0, null=3)) == 0
+
+
+def topk_args(B=2, D=3, V=100, K=4, null=None):
+    ptrs = [FAKE] * 3
+    if null is not None:
+        ptrs[null] = 0
+    return [ptrs[0], B, D, V, K, ptrs[1], ptrs[2], 0]
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), -2), (dict(K=33), -2), (dict(V=3, K=4), -2), (dict(D=0), -2), (dict(D=65), -2),
+    (dict(B=1 << 30, D=4), -2), (dict(B=-1), -1), (dict(V=0), -1),
+    (dict(null=0), -1), (dict(null=1), -1), (dict(null=2), -1)])
+def test_draft_topk_rejects_bad_arguments(lib, kw, code):
+    assert lib.ddtree_draft_topk(*topk_args(**kw)) == code
+
+
+def test_draft_topk_empty_batch_is_a_noop(lib):
+    assert lib.ddtree_draft_topk(*topk_args(B=0, null=0)) == 0
 
 
 def attn_args(**kw):

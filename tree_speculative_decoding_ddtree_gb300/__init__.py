@@ -1,6 +1,6 @@
 """DDTree tree-verify step on one GB300: thin Python binding of ``libddtree.so``.
 
-The four calls of the C ABI (``include/ddtree.h``) are exposed under the same
+The calls of the C ABI (``include/ddtree.h``) are exposed under the same
 names. This module only marshals arguments: it checks that tensors are CUDA,
 contiguous and of the right dtype and shape, passes their device pointers and
 the current stream, and raises :class:`DDTreeError` on a non-zero status. All
@@ -18,7 +18,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "DDTreeError", "load_library", "library_path", "ddtree_build", "tree_verify_attn",
+    "DDTreeError", "load_library", "library_path", "ddtree_draft_topk", "ddtree_build", "tree_verify_attn",
     "tree_verify_attn_workspace_size", "ddtree_accept_greedy", "ddtree_accept_sample",
     "TreeBuffers", "alloc_tree", "DEV_ERRORS", "tree_verify_attn_noalloc",
 ]
@@ -57,6 +57,8 @@ def load_library(path: Optional[str] = None):
     lib.ddtree_status_string.argtypes = [I]
     lib.ddtree_last_error.restype = ctypes.c_char_p
     lib.ddtree_last_error.argtypes = []
+    lib.ddtree_draft_topk.restype = I
+    lib.ddtree_draft_topk.argtypes = [P, I, I, I, I, P, P, P]
     lib.ddtree_build.restype = I
     lib.ddtree_build.argtypes = [P] * 4 + [I] * 4 + [P] * 10 + [P, P]
     lib.tree_verify_attn.restype = I
@@ -99,6 +101,25 @@ def _ptr(t: Optional[torch.Tensor], dtype, name: str, shape=None) -> int:
 def _stream(stream) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
+
+
+def ddtree_draft_topk(draft_logits: torch.Tensor, K: int, topk_logp: Optional[torch.Tensor] = None,
+                      topk_tok: Optional[torch.Tensor] = None, stream=None):
+    """Per-depth top-K tokens and log-probs of fp32 draft logits ``[B, D, V]``
+    (see ``ddtree_draft_topk`` in include/ddtree.h). Returns ``(topk_logp, topk_tok)``."""
+    lib = load_library()
+    B, D, V = draft_logits.shape
+    dev = draft_logits.device
+    if topk_logp is None:
+        topk_logp = torch.empty((B, D, K), dtype=torch.float32, device=dev)
+    if topk_tok is None:
+        topk_tok = torch.empty((B, D, K), dtype=torch.int32, device=dev)
+    st = lib.ddtree_draft_topk(
+        _ptr(draft_logits, torch.float32, "draft_logits", (B, D, V)), B, D, V, K,
+        _ptr(topk_logp, torch.float32, "topk_logp", (B, D, K)),
+        _ptr(topk_tok, torch.int32, "topk_tok", (B, D, K)), _stream(stream))
+    _check(st, "ddtree_draft_topk")
+    return topk_logp, topk_tok
 
 
 class TreeBuffers:

@@ -18,6 +18,7 @@ cudaError_t launch_accept_sample(const float*, int, const int32_t*, const int32_
                                  const int32_t*, const int32_t*, int, int, int, const float*,
                                  const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*,
                                  int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_draft_topk(const float*, int, int, int, int, float*, int32_t*, cudaStream_t);
 
 namespace {
 
@@ -92,6 +93,19 @@ const char* ddtree_status_string(int status) {
 }
 
 const char* ddtree_last_error(void) { return g_last_error; }
+
+int ddtree_draft_topk(const float* draft_logits, int B, int D, int V, int K, float* topk_logp,
+                      int32_t* topk_tok, void* stream) {
+    if (B < 0 || V < 1) return DDT_EINVAL;
+    if (K < 1 || K > DDT_MAX_TOPK || K > V || D < 1 || D > DDT_MAX_DEPTH ||
+        static_cast<long long>(B) * D > 0x7FFFFFFFll)
+        return DDT_ESHAPE;
+    if (B == 0) return DDT_OK;
+    if (!draft_logits || !topk_logp || !topk_tok) return DDT_EINVAL;
+    cudaError_t e = launch_draft_topk(draft_logits, V, B, D, K, topk_logp, topk_tok,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
 
 int ddtree_build(const float* topk_logp, const int32_t* topk_tok, const int32_t* root_tok,
                  const int32_t* ctx_len, int B, int D, int K, int budget, int32_t* parent,
