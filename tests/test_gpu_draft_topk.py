@@ -2,13 +2,15 @@
 
 Tokens are compared bit-exactly (the ranking is decided on the fp32 logits on
 both sides, ties to the lower id, NaN last). Log-probs: the oracle forms the
-row's log-sum-exp in fp64; the kernel sums exp(x - max) in fp32 (at most
-about V / 512 + 5 terms enter one running sum before the fp64 combine), so
-the sum carries a relative error below (V / 512 + 8) * 2^-24 plus the expf
-error of each term, and the log-sum-exp an absolute error of the same size;
-rounding the fp64 log-prob to fp32 adds half an ulp. The bar below,
-|got - ref| <= (V / 512 + 64) * 2^-22 + 2^-23 |ref|, is that bound with a
-factor of 2 or more to spare.
+row's log-sum-exp in fp64. The kernel sums exp(x - max) in fp32 with the
+__expf intrinsic (documented error: 2 ulp plus about 1.2 |x| ulp), at most
+V / 512 + 16 terms per running sum, then combines 16 warp partials and takes
+logf. Relative to the exp-sum S >= 1, the per-term errors weigh at most
+(2 + 1.6 (ln V + 1)) ulp (terms with |x| > ln V + 1 are below 1/(eV) each),
+the running sums and the combine (V / 512 + 37) ulp, and logf one ulp of
+log S <= 16 ulp; rounding the fp64 log-prob to fp32 adds half an ulp of it.
+The bar below, |got - ref| <= (V / 512 + 64) * 2^-22 + 2^-23 |ref|, is that
+bound with a factor of 3 or more to spare.
 """
 import numpy as np
 import pytest
@@ -123,6 +125,36 @@ def test_draft_topk_unaligned_rows_take_the_scalar_path():
     view = buf[1:].view(B, D, V)   # 4-byte aligned, not 16-byte aligned
     assert view.data_ptr() % 16 != 0
     check(x, 8, x_dev=view)
+
+
+# Share layout of the kernel (512 threads, 4 units of 16 bytes, or of one
+# float when V % 4 != 0, in flight per thread): thread (warp w, lane l) reads
+# units w * 128 + l + it * 2048 + j * 32 (j < 4). The test below fills whole
+# shares of six threads with large values, so that more than 1024 elements
+# pass the threshold and the kernel takes its exact many-candidates path.
+def _share(w, l, n_units, per_unit):
+    units = [w * 128 + l + it * 2048 + j * 32 for it in range(n_units // 2048 + 1) for j in range(4)]
+    units = [u for u in units if u < n_units]
+    return np.array([u * per_unit + e for u in units for e in range(per_unit)])
+
+
+@pytest.mark.parametrize("V", [131072, 131071])
+def test_draft_topk_many_candidates_path(V):
+    rng = np.random.default_rng(V)
+    per_unit = 4 if V % 4 == 0 else 1
+    n_units = V // per_unit
+    x = rng.standard_normal((1, 2, V)).astype(np.float32)
+    for d in range(2):
+        for t in range(6):   # six whole shares above the threshold
+            idx = _share(0, t, n_units, per_unit)
+            assert len(idx) >= 200
+            x[0, d, idx] = rng.uniform(600, 1000, len(idx)).astype(np.float32)
+        for t in range(2):   # two more best elements set the threshold near 500
+            idx = _share(1, t, n_units, per_unit)
+            x[0, d, idx[5]] = np.float32(500 + t)
+    x[0, 1, _share(0, 3, n_units, per_unit)] = np.float32(700.0)   # ties inside a share
+    check(x, 8)
+    check(x, 32)
 
 
 def test_draft_topk_feeds_the_build():

@@ -8,21 +8,44 @@
 // Ranking is by the logit (the log-prob order), ties to the lower token id;
 // log-prob = logit - log(sum exp(logits)) of the row.
 //
-// One CTA per (request, depth) row. Each thread streams its share of the row
-// (16-byte loads) keeping an online (max, sum of exp(x - max)) pair for the
-// log-sum-exp, and each warp keeps the row's K best keys seen so far spread
-// over its lanes (lane k holds the k-th best): a value above the K-th best is
-// inserted with one ballot and one shift. Keys pack the logit's order key
-// above the inverted token id, so a larger key is a larger logit or, on a
-// tie, a lower id; NaN ranks below every number. Warp 0 merges the warps'
-// lists. The log-sum-exp is combined in fp64 and the log-probs are formed in
-// fp64, then rounded to fp32.
+// One CTA per (request, depth) row; the row is read once from HBM.
+//  Pass A: every thread streams its share of the row (16-byte loads, several
+//    in flight) keeping an online (max, sum of exp(x - max)) pair for the
+//    log-sum-exp; the max with its lowest id is the thread's best element. A key packs the logit's
+//    order key above the inverted token id, so a larger key is a larger logit
+//    or, on a tie, a lower id; NaN ranks below every number.
+//  Threshold: T = the K-th largest of the threads' best keys (a bitonic sort
+//    per warp, then ranks across warps). At least K elements have a key >= T,
+//    so every element of the top K has a key >= T and sits in a thread whose
+//    best key is >= T: exactly K threads, keys being distinct.
+//  Pass B: the warps re-read those threads' shares (from L2, one unit per
+//    lane) and stage the elements with key >= T in shared memory; the K largest staged keys, ranked by
+//    counting, are the answer. Rows with more candidates than the staging
+//    array holds (many equal logits) take a slower exact path instead: a
+//    sorted top-K list per warp, updated by ballot and shift, then merged.
+// The exp-sum is accumulated and combined in fp32; the log-probs are formed
+// as logit - (max + log(sum)) in fp64, then rounded to fp32.
 #include "common.cuh"
 
 namespace ddt {
 
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkCap = 1024;   // staged candidate keys
+constexpr int kTopkUnroll = 4;   // loads in flight per thread (4 measured best of 4, 8, 16)
+
+// descending bitonic sort of one key per lane across the warp
+DDT_DEVINL unsigned long long warp_sort_desc(unsigned long long v, int lane) {
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+            v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+        }
+    return v;
+}
 
 // insert key k into the warp's sorted list (lanes 0..K-1, descending); k is
 // larger than the K-th key and differs from every key in the list
@@ -47,128 +70,266 @@ DDT_DEVINL void list_offer(unsigned long long& list, unsigned long long& thr, un
     }
 }
 
-// online (max, sum of exp(x - max)) of a row share; NaN only sets the flag
-// (the row's log-sum-exp is then NaN, as is the case for a +inf or all -inf row)
-struct Lse {
-    float m, s;
-    bool nan;
-};
-
-DDT_DEVINL Lse lse_merge(Lse a, Lse b) {
-    Lse r;
-    r.nan = a.nan || b.nan;
-    r.m = fmaxf(a.m, b.m);
-    if (r.m == -INFINITY || r.m == INFINITY) {
-        r.s = 0.0f;   // only the flagged cases reach here with a non-empty share
-    } else {
-        r.s = (a.s > 0.0f ? a.s * expf(a.m - r.m) : 0.0f) + (b.s > 0.0f ? b.s * expf(b.m - r.m) : 0.0f);
-    }
-    return r;
-}
-
-// kL floats per load (4: 16-byte loads, needs V % 4 == 0 and an aligned row),
-// kU loads in flight per lane
-template <int kL>
-__global__ void __launch_bounds__(kTopkThreads)
-draft_topk_kernel(const float* __restrict__ logits, int V, int K,
-                  float* __restrict__ out_lp, int32_t* __restrict__ out_tok) {
-    constexpr int kU = 4;
-    __shared__ unsigned long long s_keys[kTopkWarps][DDT_MAX_TOPK];
-    __shared__ float s_m[kTopkWarps], s_s[kTopkWarps];
-    __shared__ int s_nan[kTopkWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const size_t row = blockIdx.x;
-    const float* x = logits + row * static_cast<size_t>(V);
-    const int n_units = V / kL;
-    unsigned long long list = 0ull, thr = 0ull;   // every element's key is > 0
-    Lse acc{-INFINITY, 0.0f, false};
-    // warp-uniform trip count: the list operations always see all 32 lanes
-    for (int base = warp * 32 * kU; base < n_units; base += kTopkThreads * kU) {
+// The calling thread's share of the row: units (one float4, or one float)
+// first + it * kTopkThreads * kU + j * 32 for j < kU. fn(f, g) sees each group
+// of kU loaded units, g[j] the unit index (>= n_units: absent, f = -inf).
+template <int kL, int kU, class Fn>
+DDT_DEVINL void scan_share(const float* __restrict__ x, int n_units, int first, Fn&& fn) {
+    for (int base = first; base < n_units; base += kTopkThreads * kU) {
         float f[kU][kL];
+        int g[kU];
 #pragma unroll
         for (int j = 0; j < kU; ++j) {
-            const int g = base + j * 32 + lane;
-            if (g < n_units) {
+            g[j] = base + j * 32;
+            if (g[j] < n_units) {
                 if constexpr (kL == 4) {
-                    const float4 t = __ldg(reinterpret_cast<const float4*>(x) + g);
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(x) + g[j]);
                     f[j][0] = t.x; f[j][1] = t.y; f[j][2] = t.z; f[j][3] = t.w;
                 } else {
-                    f[j][0] = __ldg(x + g);
+                    f[j][0] = __ldg(x + g[j]);
                 }
             } else {
 #pragma unroll
                 for (int e = 0; e < kL; ++e) f[j][e] = -INFINITY;   // adds nothing to the sum
             }
         }
-        float mloc = -INFINITY;
-        bool nanloc = false;
+        fn(f, g);
+    }
+}
+
+// ranks of the first K entries of each warp's descending list among all lists
+// (an entry's own list counts its p predecessors): one binary search per list,
+// all lists stepped together; calls out(rank, key) for every non-zero entry
+template <class Out>
+DDT_DEVINL void rank_lists(const unsigned long long (*keys)[32], int K, Out&& out) {
+    if (threadIdx.x < kTopkWarps * K) {
+        const int w = threadIdx.x / K, p = threadIdx.x - w * K;
+        const unsigned long long c = keys[w][p];
+        int pos[kTopkWarps];
 #pragma unroll
-        for (int j = 0; j < kU; ++j)
+        for (int w2 = 0; w2 < kTopkWarps; ++w2) pos[w2] = 0;
 #pragma unroll
-            for (int e = 0; e < kL; ++e) {
-                nanloc |= f[j][e] != f[j][e];
-                mloc = fmaxf(mloc, f[j][e]);   // fmaxf skips NaN
-            }
-        const float m_new = fmaxf(acc.m, mloc);
-        if (m_new != -INFINITY) {
-            float s = acc.s > 0.0f ? acc.s * expf(acc.m - m_new) : 0.0f;
+        for (int step = 16; step > 0; step >>= 1)
+#pragma unroll
+            for (int w2 = 0; w2 < kTopkWarps; ++w2)
+                pos[w2] += keys[w2][pos[w2] + step - 1] > c ? step : 0;
+        // the steps reach 0..31; a list with all 32 keys above c counts 32
+        int rank = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kTopkWarps; ++w2) rank += pos[w2] + (keys[w2][pos[w2]] > c ? 1 : 0);
+        if (c != 0ull) out(rank, c);
+    }
+}
+
+template <int kL>
+__global__ void __launch_bounds__(kTopkThreads)
+draft_topk_kernel(const float* __restrict__ logits, int V, int K, float* __restrict__ out_lp,
+                  int32_t* __restrict__ out_tok) {
+    constexpr int kU = kTopkUnroll;
+    __shared__ unsigned long long s_keys[kTopkWarps][32];
+    __shared__ unsigned long long s_cand[kTopkCap];
+    __shared__ float s_m[kTopkWarps], s_s[kTopkWarps];
+    __shared__ int s_nan[kTopkWarps];
+    __shared__ uint32_t s_win[32];
+    __shared__ int s_sel[32];
+    __shared__ unsigned long long s_T;
+    __shared__ int s_count;
+    __shared__ double s_lse;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const size_t row = blockIdx.x;
+    const float* x = logits + row * static_cast<size_t>(V);
+    const int n_units = V / kL;
+    const int first = warp * 32 * kU + lane;
+
+    // pass A: exp-sum, and the thread's best element (the exp-sum's running
+    // max; its lowest id is searched for only when a group raises the max)
+    float m = -INFINITY, s = 0.0f;
+    bool nan = false;
+    uint32_t best_i = 0u;
+    scan_share<kL, kU>(x, n_units, first, [&](const float (&f)[kU][kL], const int (&g)[kU]) {
+        float mj[kL];   // kL independent chains; fmaxf skips NaN
+#pragma unroll
+        for (int e = 0; e < kL; ++e) mj[e] = f[0][e];
+#pragma unroll
+        for (int j = 1; j < kU; ++j)
+#pragma unroll
+            for (int e = 0; e < kL; ++e) mj[e] = fmaxf(mj[e], f[j][e]);
+        float mloc = mj[0];
+#pragma unroll
+        for (int e = 1; e < kL; ++e) mloc = fmaxf(mloc, mj[e]);
+        if (mloc > m) {
+            bool found = false;   // the first (lowest id) element equal to the new max
 #pragma unroll
             for (int j = 0; j < kU; ++j)
 #pragma unroll
-                for (int e = 0; e < kL; ++e) s += expf(f[j][e] - m_new);
-            acc.s = s;
-            acc.m = m_new;
+                for (int e = 0; e < kL; ++e)
+                    if (!found && f[j][e] == mloc) {
+                        found = true;
+                        best_i = static_cast<uint32_t>(g[j] * kL + e);
+                    }
+            s = s != 0.0f ? s * __expf(m - mloc) : 0.0f;
+            m = mloc;
         }
-        acc.nan |= nanloc;
+        if (m != -INFINITY) {
+            float t[kL];   // kL independent chains; a NaN makes the sum NaN
 #pragma unroll
-        for (int j = 0; j < kU; ++j) {
-            const int g = base + j * 32 + lane;
+            for (int e = 0; e < kL; ++e) t[e] = __expf(f[0][e] - m);
 #pragma unroll
-            for (int e = 0; e < kL; ++e) {
-                const unsigned long long key =
-                    g < n_units ? argmax_pack(float_order_key(f[j][e]), static_cast<uint32_t>(g * kL + e)) : 0ull;
-                list_offer(list, thr, key, K, lane);
+            for (int j = 1; j < kU; ++j)
+#pragma unroll
+                for (int e = 0; e < kL; ++e) t[e] += __expf(f[j][e] - m);
+#pragma unroll
+            for (int e = 1; e < kL; ++e) t[0] += t[e];
+            s += t[0];
+        } else {
+#pragma unroll
+            for (int j = 0; j < kU; ++j)
+#pragma unroll
+                for (int e = 0; e < kL; ++e) nan |= f[j][e] != f[j][e];
+        }
+    });
+    unsigned long long my_key = 0ull;
+    if (m != -INFINITY) {
+        my_key = argmax_pack(float_order_key(m), best_i);
+    } else if (first < n_units) {
+        // every element of the share is -inf or NaN: the best is the first -inf,
+        // else the first NaN (NaN ranks lowest)
+        uint32_t first_ninf = 0xFFFFFFFFu;
+        scan_share<kL, kU>(x, n_units, first, [&](const float (&f)[kU][kL], const int (&g)[kU]) {
+#pragma unroll
+            for (int j = 0; j < kU; ++j)
+#pragma unroll
+                for (int e = 0; e < kL; ++e)
+                    if (g[j] < n_units && f[j][e] == -INFINITY && first_ninf == 0xFFFFFFFFu)
+                        first_ninf = static_cast<uint32_t>(g[j] * kL + e);
+        });
+        my_key = first_ninf != 0xFFFFFFFFu ? argmax_pack(float_order_key(-INFINITY), first_ninf)
+                                           : argmax_pack(0u, static_cast<uint32_t>(first * kL));
+    }
+
+    // warp partial of the exp-sum
+    {
+        const float mw = warp_max_f(m);
+        float t = 0.0f;
+        if (mw != -INFINITY && mw != INFINITY && m != -INFINITY) t = s * __expf(m - mw);   // NaN s propagates
+        t = warp_sum_f(t);
+        nan = __any_sync(0xffffffffu, nan);
+        if (lane == 0) { s_m[warp] = mw; s_s[warp] = t; s_nan[warp] = nan; }
+    }
+    s_keys[warp][lane] = warp_sort_desc(my_key, lane);
+    if (threadIdx.x < 32) { s_win[threadIdx.x] = 0u; s_sel[threadIdx.x] = -1; }
+    if (threadIdx.x == 0) { s_T = 0ull; s_count = 0; }
+    __syncthreads();
+
+    if (warp == kTopkWarps - 1) {   // the row's log-sum-exp (beside the ranks below)
+        const float mw = lane < kTopkWarps ? s_m[lane] : -INFINITY;
+        const float sw = lane < kTopkWarps ? s_s[lane] : 0.0f;
+        const bool any_nan = __any_sync(0xffffffffu, lane < kTopkWarps && s_nan[lane] != 0);
+        const float M = warp_max_f(mw);
+        float term = 0.0f;
+        if (M != -INFINITY && M != INFINITY && sw != 0.0f) term = sw * expf(mw - M);
+        term = warp_sum_f(term);
+        if (lane == 0)
+            s_lse = (any_nan || M == -INFINITY || M == INFINITY)
+                        ? __longlong_as_double(0x7FF8000000000000ll)   // NaN, as the exp-sum is
+                        : static_cast<double>(M) + static_cast<double>(logf(term));
+    }
+    // T = the K-th largest best key (stays 0 if fewer than K threads hold
+    // elements); the threads holding the K largest best keys are selected. A
+    // key's unit g = id / kL belongs to thread (warp, lane) with lane = g % 32
+    // and warp = (g % (kTopkThreads * kU)) / (32 * kU).
+    rank_lists(s_keys, K, [&](int rank, unsigned long long c) {
+        if (rank < K) {
+            const uint32_t g = argmax_unpack_idx(c) / kL;
+            s_sel[rank] = static_cast<int>((g % (kTopkThreads * kU)) / (32 * kU) * 32 + g % 32);
+        }
+        if (rank == K - 1) s_T = c;
+    });
+    __syncthreads();
+    const unsigned long long T = s_T;
+
+    // pass B: each warp re-reads selected shares, one unit per lane, and
+    // stages the keys >= T
+    for (int q = warp; q < K; q += kTopkWarps) {
+        const int tid = s_sel[q];
+        if (tid < 0) continue;
+        const int t_first = (tid >> 5) * 32 * kU + (tid & 31);
+        for (int i0 = 0;; i0 += 32) {
+            const int i = i0 + lane;
+            // unit i of the share: group i / kU, slot i % kU
+            if (static_cast<long long>(t_first) + static_cast<long long>(i0 / kU) * kTopkThreads * kU >= n_units)
+                break;   // warp-uniform: no unit of this or a later batch exists
+            const long long g = static_cast<long long>(t_first) +
+                                static_cast<long long>(i / kU) * kTopkThreads * kU + (i % kU) * 32;
+            if (g < n_units) {
+                float f[kL];
+                if constexpr (kL == 4) {
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(x) + g);
+                    f[0] = t.x; f[1] = t.y; f[2] = t.z; f[3] = t.w;
+                } else {
+                    f[0] = __ldg(x + g);
+                }
+#pragma unroll
+                for (int e = 0; e < kL; ++e) {
+                    const unsigned long long k =
+                        argmax_pack(float_order_key(f[e]), static_cast<uint32_t>(g * kL + e));
+                    if (k >= T) {
+                        const int slot = atomicAdd(&s_count, 1);
+                        if (slot < kTopkCap) s_cand[slot] = k;
+                    }
+                }
             }
         }
     }
-    // warp partials of the log-sum-exp
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        Lse other;
-        other.m = __shfl_xor_sync(0xffffffffu, acc.m, o);
-        other.s = __shfl_xor_sync(0xffffffffu, acc.s, o);
-        other.nan = __shfl_xor_sync(0xffffffffu, static_cast<int>(acc.nan), o) != 0;
-        acc = lse_merge(acc, other);
-    }
-    if (lane < K) s_keys[warp][lane] = list;
-    if (lane == 0) { s_m[warp] = acc.m; s_s[warp] = acc.s; s_nan[warp] = acc.nan; }
     __syncthreads();
-    if (warp != 0) return;
-    // warp 0: merge the other warps' lists into its own (warp 0 has seen at
-    // least min(V, 32) >= K elements, so its list is full and thr > 0: the
-    // empty slots of shorter lists, key 0, never enter)
-    for (int w = 1; w < kTopkWarps; ++w) {
-        const unsigned long long cand = lane < K ? s_keys[w][lane] : 0ull;
-        list_offer(list, thr, cand, K, lane);
-    }
-    bool nan = false;
-    float M = -INFINITY;
-    for (int w = 0; w < kTopkWarps; ++w) { M = fmaxf(M, s_m[w]); nan |= s_nan[w] != 0; }
-    double lse;
-    if (nan || M == -INFINITY || M == INFINITY) {
-        lse = __longlong_as_double(0x7FF8000000000000ll);   // NaN, as the row's exp-sum is
+    const int n = s_count;
+    if (n <= kTopkCap) {
+        // exact ranks among the staged keys (distinct; at least K of them)
+        for (int c = threadIdx.x; c < n; c += kTopkThreads) {
+            const unsigned long long key = s_cand[c];
+            int rank = 0;
+            for (int i = 0; i < n; ++i) rank += s_cand[i] > key;
+            if (rank < K) s_win[rank] = argmax_unpack_idx(key);
+        }
     } else {
-        double s = 0.0;
-        for (int w = 0; w < kTopkWarps; ++w)
-            if (s_s[w] > 0.0f)
-                s += static_cast<double>(s_s[w]) * exp(static_cast<double>(s_m[w]) - static_cast<double>(M));
-        lse = static_cast<double>(M) + log(s);
+        // many candidates: a sorted list per warp over the whole row (keys < T
+        // dropped), then the lists' ranks
+        unsigned long long list = 0ull, thr = 0ull;   // every element's key is > 0
+        for (int base = warp * 32 * kU; base < n_units; base += kTopkThreads * kU) {
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+                const int g = base + j * 32 + lane;
+                float f[kL];
+                if (g < n_units) {
+                    if constexpr (kL == 4) {
+                        const float4 t = __ldg(reinterpret_cast<const float4*>(x) + g);
+                        f[0] = t.x; f[1] = t.y; f[2] = t.z; f[3] = t.w;
+                    } else {
+                        f[0] = __ldg(x + g);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < kL; ++e) {
+                    unsigned long long key = 0ull;
+                    if (g < n_units) {
+                        key = argmax_pack(float_order_key(f[e]), static_cast<uint32_t>(g * kL + e));
+                        if (key < T) key = 0ull;
+                    }
+                    list_offer(list, thr, key, K, lane);
+                }
+            }
+        }
+        s_keys[warp][lane] = lane < K ? list : 0ull;   // the earlier readers are past a barrier
+        __syncthreads();
+        rank_lists(s_keys, K, [&](int rank, unsigned long long c) {
+            if (rank < K) s_win[rank] = argmax_unpack_idx(c);
+        });
     }
-    if (lane < K) {
-        const uint32_t idx = argmax_unpack_idx(list);
-        const float v = __ldg(x + idx);
-        out_tok[row * K + lane] = static_cast<int32_t>(idx);
-        out_lp[row * K + lane] = static_cast<float>(static_cast<double>(v) - lse);
+    __syncthreads();
+    if (threadIdx.x < K) {
+        const uint32_t idx = s_win[threadIdx.x];
+        out_tok[row * K + threadIdx.x] = static_cast<int32_t>(idx);
+        out_lp[row * K + threadIdx.x] = static_cast<float>(static_cast<double>(__ldg(x + idx)) - s_lse);
     }
 }
 
