@@ -580,3 +580,45 @@ def accept_sample(logits: np.ndarray, tree: Tree, D: int, temperature: np.ndarra
             nodes[b, k + 1] = c
         toks[b, len(path)] = bonus[b]
     return Accept(acc, toks, nodes, bonus, margin)
+
+
+# ----------------------------------------------------------------------------
+# commit: the verified path's K/V appended to the paged cache
+# ----------------------------------------------------------------------------
+
+def commit_kv(k_tree, v_tree, out_nodes, accept_len, ctx_len, page_table, k_cache, v_cache,
+              page_size):
+    """Append each request's committed path K/V to its paged cache.
+
+    [Arch] §"Section 1", step 5: only the single longest verified path is
+    committed; the other tree nodes are dropped. [Branch] §"Hypothesis 3": a
+    node of depth d was verified at position ``ctx_len + d``.
+
+    Reading (pages silent on the cache write): the committed rows are the
+    root (tree row 0, whose K/V the verify pass computed at position
+    ``ctx_len``) followed by the accepted nodes in path order, i.e.
+    ``out_nodes[b, 0..accept_len[b]]``; path row i is written to token
+    position ``ctx_len[b] + i`` (slot ``t % page_size`` of page
+    ``page_table[b, t // page_size]``), which is its depth, so the position it
+    was verified at. The bonus token is not written: it is the next step's
+    root and its K/V comes from that pass. ``new_ctx_len = ctx_len +
+    accept_len + 1``.
+
+    Works on any element type (the bf16 bit patterns are copied as they are).
+    Returns ``(k_cache', v_cache', new_ctx_len)`` as new arrays.
+    """
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    B = k_tree.shape[0]
+    new_ctx = np.array(ctx_len, dtype=np.int32, copy=True)
+    for b in range(B):
+        a = int(accept_len[b])
+        for i in range(a + 1):
+            node = int(out_nodes[b, i])
+            t = int(ctx_len[b]) + i
+            page = int(page_table[b, t // page_size])
+            slot = t % page_size
+            kc[page, slot] = k_tree[b, node]
+            vc[page, slot] = v_tree[b, node]
+        new_ctx[b] = int(ctx_len[b]) + a + 1
+    return kc, vc, new_ctx

@@ -571,3 +571,87 @@ def test_build_equal_scores_follow_push_order():
     assert t.parent[0].tolist() == [-1, 0, 1]
     t3 = O.build_tree(lp, tok, np.array([0]), np.array([0]), 3)
     assert t3.token[0].tolist() == [0, 1, 3, 2]
+
+
+# ---------------------------------------------------------------------------
+# commit of the verified path's K/V
+# ---------------------------------------------------------------------------
+
+def test_commit_hand_worked_example():
+    # page_size 4, request 0 owns pages [2, 0, 1] (tokens 0-3 on page 2, 4-7 on
+    # page 0, 8-11 on page 1) and holds 3 tokens; the path is rows 0, 2, 5
+    # (accept_len 2). Worked by hand: token 3 -> page 2 slot 3, token 4 ->
+    # page 0 slot 0, token 5 -> page 0 slot 1; the new length is 6.
+    N, Hkv, Dh = 6, 1, 2
+    k_tree = np.arange(1, N + 1, dtype=np.float64)[None, :, None, None] * np.ones((1, N, Hkv, Dh))
+    v_tree = -k_tree
+    k_cache = np.zeros((3, 4, Hkv, Dh))
+    v_cache = np.zeros((3, 4, Hkv, Dh))
+    kc, vc, new_ctx = O.commit_kv(k_tree, v_tree, np.array([[0, 2, 5, -1]]), np.array([2]),
+                                  np.array([3]), np.array([[2, 0, 1]]), k_cache, v_cache, 4)
+    assert new_ctx.tolist() == [6]
+    expect = np.zeros((3, 4))
+    expect[2, 3], expect[0, 0], expect[0, 1] = 1.0, 3.0, 6.0   # rows 0, 2, 5 hold 1, 3, 6
+    assert np.array_equal(kc[:, :, 0, 0], expect) and np.array_equal(kc[:, :, 0, 1], expect)
+    assert np.array_equal(vc[:, :, 0, 0], -expect)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_commit_appends_the_path_to_the_token_sequence(seed):
+    # the cache read as a token sequence after the commit is the old sequence
+    # followed by the path rows in path order; no other slot changes
+    rng = np.random.default_rng(seed)
+    B, N, Hkv, Dh, page, D = 3, 9, 2, 4, 4, 4
+    ctx = rng.integers(0, 12, B).astype(np.int32)
+    max_pages = 5
+    table = rng.permutation(B * max_pages).reshape(B, max_pages).astype(np.int32)
+    k_cache = rng.standard_normal((B * max_pages, page, Hkv, Dh))
+    v_cache = rng.standard_normal((B * max_pages, page, Hkv, Dh))
+    k_tree = rng.standard_normal((B, N, Hkv, Dh))
+    v_tree = rng.standard_normal((B, N, Hkv, Dh))
+    acc = rng.integers(0, D + 1, B).astype(np.int32)
+    nodes = np.full((B, D + 1), -1, np.int32)
+    for b in range(B):
+        nodes[b, 0] = 0
+        nodes[b, 1:acc[b] + 1] = np.sort(rng.choice(np.arange(1, N), acc[b], replace=False))
+    kc, vc, new_ctx = O.commit_kv(k_tree, v_tree, nodes, acc, ctx, table, k_cache, v_cache, page)
+    assert np.array_equal(new_ctx, ctx + acc + 1)
+    for b in range(B):
+        path = nodes[b, :acc[b] + 1]
+        for old, new, tree in ((k_cache, kc, k_tree), (v_cache, vc, v_tree)):
+            seq_old = O.gather_context(old, table, b, int(ctx[b]), page)
+            seq_new = O.gather_context(new, table, b, int(new_ctx[b]), page)
+            assert np.array_equal(seq_new, np.concatenate([seq_old, tree[b, path]], axis=0))
+    touched = np.zeros(k_cache.shape[:2], bool)
+    for b in range(B):
+        for t in range(int(ctx[b]), int(new_ctx[b])):
+            touched[table[b, t // page], t % page] = True
+    assert np.array_equal(kc[~touched], k_cache[~touched])
+    assert np.array_equal(vc[~touched], v_cache[~touched])
+
+
+def test_commit_of_a_chain_is_the_linear_dflash_commit():
+    # top-k 1: the tree is the D-node chain (node index = depth), the greedy
+    # walk accepts a prefix, and the commit appends verify rows 0..a in order
+    w = S.config("tiny")
+    dl, root, _ = S.draft_inputs(w)
+    lp, tok = O.draft_topk(dl, 1)
+    ctx = np.array([5], np.int32)
+    tree = O.build_tree(lp, tok, root, ctx, w.D)
+    assert tree.parent[0, 1:].tolist() == list(range(w.D))
+    logits = np.zeros((1, w.D + 1, w.V))
+    for d in range(w.D):   # the target agrees with the first three draft tokens
+        logits[0, d, tree.token[0, d + 1] if d < 3 else (tree.token[0, d + 1] + 1) % w.V] = 1.0
+    acc = O.accept_greedy(logits, tree, w.D)
+    assert int(acc.accept_len[0]) == 3
+    rng = np.random.default_rng(0)
+    k_tree = rng.standard_normal((1, w.D + 1, 1, 4))
+    v_tree = rng.standard_normal((1, w.D + 1, 1, 4))
+    k_cache = rng.standard_normal((4, 4, 1, 4))
+    v_cache = rng.standard_normal((4, 4, 1, 4))
+    table = np.array([[3, 1, 0, 2]], np.int32)
+    kc, _, new_ctx = O.commit_kv(k_tree, v_tree, acc.out_nodes, acc.accept_len, ctx, table,
+                                 k_cache, v_cache, 4)
+    assert new_ctx.tolist() == [9]
+    seq = O.gather_context(kc, table, 0, 9, 4)
+    assert np.array_equal(seq[5:9], k_tree[0, 0:4])
