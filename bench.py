@@ -5,7 +5,9 @@ One step = the whole hot path over one batch: ddtree_build -> tree_verify_attn
 same tree at T = 0.7, as a server would for the temperature requests of a
 batch; the two walks are independent and run concurrently on two streams).
 The step's input, the per-depth top-k, is made once by ddtree_draft_topk
-from the draft logits; that call is timed on its own (`per_call_us`).
+from the draft logits; that call, ddtree_commit_kv and the library's own
+step graph (build, attention, greedy walk, commit: ddtree_step_*) are timed
+on their own (`per_call_us`).
 
 The default workload is the batched serving case: 16 requests with contexts
 uniform in [1024, 16384] tokens (paged, page 64, shuffled pages), 64 query /
@@ -72,7 +74,7 @@ def make_host_inputs(w):
     import ddtree_synth as S
     dl, root, _ = S.draft_inputs(w)
     ctx = S.context_lengths(w)
-    table, npg = S.paged_layout(w, ctx)
+    table, npg = S.paged_layout(w, ctx, room=w.D + 1)   # pages for the commit to write into
     qkv = S.qkv_tree(w)
     kv = S.kv_cache(w, npg)
     import dataclasses
@@ -384,8 +386,17 @@ def run_native(args):
                     fn()
         return gr
 
+    # the commit and the whole step as the library's own graph: the new lengths
+    # go to a scratch array, so every launch commits the same rows
+    commit_ctx = torch.empty_like(ctx)
+    native_step = dd.VerifyStep(topk_logp=topk_logp, topk_tok=topk_tok, root_tok=root, ctx_len=ctx, q=q,
+                                k_tree=k_tree, v_tree=v_tree, k_cache=k_cache, v_cache=v_cache,
+                                page_table=table, logits=logits, budget=w.budget, scale=scale,
+                                new_ctx_len=commit_ctx, dev_status=status)
     calls = {
         "ddtree_draft_topk": lambda: dd.ddtree_draft_topk(dl_d, w.K, topk_logp, topk_tok),
+        "ddtree_commit_kv": lambda: dd.ddtree_commit_kv(k_tree, v_tree, go, ctx, table, k_cache, v_cache,
+                                                        new_ctx_len=commit_ctx, dev_status=status),
         "ddtree_build": lambda: dd.ddtree_build(topk_logp, topk_tok, root, ctx, w.budget, out=tree,
                                                 dev_status=status),
         "tree_verify_attn": lambda: dd.tree_verify_attn(q, k_tree, v_tree, k_cache, v_cache, table, ctx,
@@ -441,6 +452,18 @@ def run_native(args):
         e1.record(stream)
         torch.cuda.synchronize()
         per_call_us[n] = e0.elapsed_time(e1) * 1e3 / 50
+    # the library's step graph, launched directly (a graph launch per step)
+    for _ in range(3):
+        native_step.launch()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(50):
+        native_step.launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    per_call_us["ddtree_step_graph"] = e0.elapsed_time(e1) * 1e3 / 50
     if world > 1:
         tt = torch.tensor([elapsed_ms], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)

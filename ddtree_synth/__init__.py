@@ -150,17 +150,18 @@ def context_lengths(w: Workload) -> np.ndarray:
     return rng.integers(w.ctx_lo, w.ctx_hi + 1, size=w.B, dtype=np.int64).astype(np.int32)
 
 
-def paged_layout(w: Workload, ctx_len: np.ndarray, spare_pages: int = 0):
+def paged_layout(w: Workload, ctx_len: np.ndarray, spare_pages: int = 0, room: int = 0):
     """Page table int32 ``[B, max_pages]`` and the pool size.
 
-    Request b owns ``ceil(ctx_len[b] / page_size)`` pages. With
+    Request b owns ``ceil((ctx_len[b] + room) / page_size)`` pages (``room``
+    token positions past the context, for a commit to write into). With
     ``paged_shuffle`` the pool's pages are handed out in a random order,
     otherwise in order (an identity layout for one contiguous context).
     Unused table entries hold -1. ``spare_pages`` extra pool pages are never
     referenced.
     """
     ps = w.page_size
-    need = [-(-int(L) // ps) for L in ctx_len]
+    need = [-(-(int(L) + room) // ps) for L in ctx_len]
     total = sum(need) + spare_pages
     order = np.arange(total, dtype=np.int64)
     if w.paged_shuffle:

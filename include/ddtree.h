@@ -13,6 +13,9 @@
  *   ddtree_accept_sample  the same at temperature, by recursive rejection
  *                         sampling over siblings + a bonus from the residual
  *
+ * and ddtree_commit_kv appends the committed path's K/V to the paged cache;
+ * ddtree_step_* records build -> attention -> walk -> commit as one graph.
+ *
  * Sources (page titles; sections named at each call):
  *   [Arch]   "The Architecture of Speculative Decoding: Dissecting DDTree's
  *            Tree-Parallel Evaluation Strategy"
@@ -279,6 +282,112 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                          uint64_t philox_offset, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
                          int32_t* dev_status, void* stream);
+
+/*
+ * ddtree_commit_kv - append the committed path's K/V to the paged cache.
+ *
+ * [Arch] Section 1, step 5: only the single longest verified path is
+ * committed; the other tree nodes are dropped. [Branch] Hypothesis 3: a node
+ * of depth d was verified at position ctx_len + d. Path row i (i = 0 is the
+ * root, whose K/V this verify pass computed, then the accepted nodes) is
+ * written to token position t = ctx_len[b] + i, i.e. slot t % page_size of
+ * page page_table[b, t / page_size]. The bonus token is not written: it is
+ * the next step's root. Then new_ctx_len[b] = ctx_len[b] + accept_len[b] + 1.
+ *
+ * Inputs
+ *   k_tree, v_tree  bf16 [B, N, Hkv, Dh]   as given to tree_verify_attn
+ *   out_nodes       int32 [B, D+1]         from either accept walk
+ *   accept_len      int32 [B]
+ *   page_table      int32 [B, max_pages]   must already map the positions up
+ *                                          to ctx_len + accept_len
+ *   ctx_len         int32 [B]
+ * In/out
+ *   k_cache, v_cache bf16 [num_pages, page_size, Hkv, Dh]: only the slots of
+ *                   the committed positions are written
+ * Outputs
+ *   new_ctx_len     int32 [B]; may be the same array as ctx_len (advanced in
+ *                   place: each request's length is read before it is
+ *                   written)
+ * The four K/V pointers must be 16-byte aligned; Hkv * Dh % 8 == 0.
+ * Device errors: accept_len outside [0, D] or a path row outside [0, N) sets
+ * DDT_DEV_BAD_TREE; ctx_len < 0 or ctx_len + accept_len + 1 beyond
+ * max_pages * page_size sets DDT_DEV_BAD_CTX; a page id outside the pool sets
+ * DDT_DEV_BAD_PAGE. Such a request writes no slot and keeps its length.
+ */
+int ddtree_commit_kv(const ddtree_bf16* k_tree, const ddtree_bf16* v_tree,
+                     const int32_t* out_nodes, const int32_t* accept_len,
+                     int B, int N, int D, int Hkv, int Dh,
+                     ddtree_bf16* k_cache, ddtree_bf16* v_cache, int num_pages,
+                     int page_size, const int32_t* page_table, int max_pages,
+                     const int32_t* ctx_len, int32_t* new_ctx_len,
+                     int32_t* dev_status, void* stream);
+
+/*
+ * ddtree_step_* - the whole verify step as one CUDA graph.
+ *
+ * [Arch] Section 1, steps 2-5 (build, one target pass over the tree, walk,
+ * commit) as a single launch. [Pivot] The Strategic Decision: the verify
+ * path is to run under CUDA graphs; [Verify] its CUDA-graph considerations:
+ * the walk stays on the GPU so that the step can be captured. Capture needs
+ * fixed shapes and no allocation or synchronisation inside, which every call
+ * here keeps. ddtree_step_create records, on a stream of its
+ * own, the calls
+ *   ddtree_build -> tree_verify_attn -> ddtree_accept_greedy (walk = 0) or
+ *   ddtree_accept_sample (walk = 1) -> ddtree_commit_kv
+ * with the arguments below (each call checks them as it does alone; the
+ * first failure is returned and no graph is kept), and instantiates the
+ * graph. ddtree_step_launch replays it on `stream`: every launch reads the
+ * arrays' current contents (the pointers are fixed at creation). The commit
+ * writes new_ctx_len, or advances ctx_len in place when new_ctx_len is NULL,
+ * so that consecutive launches decode consecutive steps.
+ * ddtree_step_create allocates the graph (host and driver memory, no device
+ * buffer); launches allocate nothing. ddtree_step_destroy frees it (NULL is
+ * ignored). A step object may be launched from one host thread at a time.
+ */
+typedef struct ddtree_step_args {
+    /* sizes */
+    int B, D, K, budget, V, Hq, Hkv, Dh, num_pages, page_size, max_pages;
+    float scale;                 /* attention scale                          */
+    int walk;                    /* 0: greedy walk, 1: sampled walk          */
+    uint64_t philox_offset;      /* sampled walk only                        */
+    /* inputs (device) */
+    const float* topk_logp;      /* [B, D, K]        ddtree_build            */
+    const int32_t* topk_tok;     /* [B, D, K]                                */
+    const int32_t* root_tok;     /* [B]                                      */
+    int32_t* ctx_len;            /* [B]              read; advanced in place */
+                                 /*                  if new_ctx_len is NULL  */
+    const ddtree_bf16* q;        /* [B, N, Hq, Dh]   tree_verify_attn        */
+    const ddtree_bf16* k_tree;   /* [B, N, Hkv, Dh]                          */
+    const ddtree_bf16* v_tree;   /* [B, N, Hkv, Dh]                          */
+    ddtree_bf16* k_cache;        /* [num_pages, page_size, Hkv, Dh]          */
+    ddtree_bf16* v_cache;        /* [num_pages, page_size, Hkv, Dh]          */
+    const int32_t* page_table;   /* [B, max_pages]                           */
+    const float* logits;         /* [B, N, V]        the walk                */
+    const float* temperature;    /* [B]              sampled walk only       */
+    const uint64_t* seed;        /* [B]              sampled walk only       */
+    /* tree (ddtree_build outputs) */
+    int32_t* parent; int32_t* depth; int32_t* token; int32_t* rank; int32_t* pos;
+    double* score; int32_t* first_child; int32_t* next_sibling;
+    uint32_t* vis; int32_t* n_nodes;
+    /* attention */
+    ddtree_bf16* attn_out;       /* [B, N, Hq, Dh]                           */
+    float* lse;                  /* [B, N, Hq] or NULL                       */
+    void* workspace;             /* tree_verify_attn_workspace_size(...)     */
+    size_t workspace_bytes;      /*   with max_ctx = max_pages * page_size   */
+    /* walk */
+    int32_t* accept_len; int32_t* out_tokens; int32_t* out_nodes; int32_t* bonus;
+    /* commit */
+    int32_t* new_ctx_len;        /* [B] or NULL (in place)                   */
+    int32_t* dev_status;         /* nullable                                 */
+} ddtree_step_args;
+
+typedef struct ddtree_step ddtree_step;
+
+/* sizeof(ddtree_step_args), for bindings that mirror the struct */
+size_t ddtree_step_args_size(void);
+int ddtree_step_create(const ddtree_step_args* args, ddtree_step** out);
+int ddtree_step_launch(ddtree_step* step, void* stream);
+void ddtree_step_destroy(ddtree_step* step);
 
 /*
  * tree_verify_attn_noalloc - tree_verify_attn without a caller workspace.

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_four_calls():
     names = declared_functions()
-    for n in ("ddtree_draft_topk", "ddtree_build", "tree_verify_attn", "ddtree_accept_greedy", "ddtree_accept_sample"):
+    for n in ("ddtree_draft_topk", "ddtree_commit_kv", "ddtree_build", "tree_verify_attn", "ddtree_accept_greedy", "ddtree_accept_sample"):
         assert n in names
 
 
@@ -91,6 +91,31 @@ def test_draft_topk_empty_batch_is_a_noop(lib):
     assert lib.ddtree_draft_topk(*topk_args(B=0, null=0)) == 0
 
 
+def commit_args(B=2, N=9, D=8, Hkv=8, Dh=128, num_pages=10, page=64, max_pages=4, null=None,
+                unaligned=None):
+    ptrs = [FAKE] * 9
+    if null is not None:
+        ptrs[null] = 0
+    if unaligned is not None:
+        ptrs[unaligned] = FAKE + 4
+    k_tree, v_tree, nodes, acc, kc, vc, table, ctx, new_ctx = ptrs
+    return [k_tree, v_tree, nodes, acc, B, N, D, Hkv, Dh, kc, vc, num_pages, page, table, max_pages,
+            ctx, new_ctx, 0, 0]
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), -1), (dict(Hkv=0), -1), (dict(Dh=0), -1), (dict(page=0), -1), (dict(max_pages=0), -1),
+    (dict(num_pages=0), -1), (dict(N=0), -2), (dict(N=129), -2), (dict(D=0), -2), (dict(D=65), -2),
+    (dict(Hkv=1, Dh=4), -2)] + [(dict(null=i), -1) for i in range(9)]
+    + [(dict(unaligned=i), -1) for i in (0, 1, 4, 5)])
+def test_commit_rejects_bad_arguments(lib, kw, code):
+    assert lib.ddtree_commit_kv(*commit_args(**kw)) == code
+
+
+def test_commit_empty_batch_is_a_noop(lib):
+    assert lib.ddtree_commit_kv(*commit_args(B=0, null=0)) == 0
+
+
 def attn_args(**kw):
     a = dict(q=FAKE, kt=FAKE, vt=FAKE, kc=FAKE, vc=FAKE, num_pages=10, page_size=64, table=FAKE,
              max_pages=256, ctx=FAKE, vis=FAKE, nn=FAKE, B=2, N=33, Hq=64, Hkv=8, Dh=128, scale=0.1,
@@ -149,3 +174,23 @@ def test_sample_rejects_missing_rng_inputs_and_large_offset(lib):
     assert lib.ddtree_accept_sample(*walk_args(sample=True, temp=0)) == -1
     assert lib.ddtree_accept_sample(*walk_args(sample=True, seed=0)) == -1
     assert lib.ddtree_accept_sample(*walk_args(sample=True, offset=1 << 56)) == -1
+
+
+def test_step_args_mirror_matches_the_c_struct(lib):
+    import tree_speculative_decoding_ddtree_gb300 as dd
+    assert lib.ddtree_step_args_size() == ctypes.sizeof(dd.StepArgs)
+
+
+def test_step_create_rejects_before_any_cuda_call(lib):
+    import tree_speculative_decoding_ddtree_gb300 as dd
+    a = dd.StepArgs()
+    a.B, a.walk = 2, 2
+    h = ctypes.c_void_p()
+    assert lib.ddtree_step_create(ctypes.byref(a), ctypes.byref(h)) == -1   # walk not 0/1
+    a.walk, a.B = 0, 0
+    assert lib.ddtree_step_create(ctypes.byref(a), ctypes.byref(h)) == -2   # empty batch
+    assert lib.ddtree_step_create(None, ctypes.byref(h)) == -1
+    assert lib.ddtree_step_create(ctypes.byref(a), None) == -1
+    assert h.value is None
+    lib.ddtree_step_destroy(None)
+    assert lib.ddtree_step_launch(None, None) == -1

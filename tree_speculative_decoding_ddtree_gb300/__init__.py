@@ -20,7 +20,8 @@ from . import _build
 __all__ = [
     "DDTreeError", "load_library", "library_path", "ddtree_draft_topk", "ddtree_build", "tree_verify_attn",
     "tree_verify_attn_workspace_size", "ddtree_accept_greedy", "ddtree_accept_sample",
-    "TreeBuffers", "alloc_tree", "DEV_ERRORS", "tree_verify_attn_noalloc",
+    "TreeBuffers", "alloc_tree", "DEV_ERRORS", "tree_verify_attn_noalloc", "ddtree_commit_kv",
+    "StepArgs", "VerifyStep",
 ]
 
 DEV_ERRORS = {
@@ -59,6 +60,16 @@ def load_library(path: Optional[str] = None):
     lib.ddtree_last_error.argtypes = []
     lib.ddtree_draft_topk.restype = I
     lib.ddtree_draft_topk.argtypes = [P, I, I, I, I, P, P, P]
+    lib.ddtree_commit_kv.restype = I
+    lib.ddtree_commit_kv.argtypes = [P, P, P, P, I, I, I, I, I, P, P, I, I, P, I, P, P, P, P]
+    lib.ddtree_step_args_size.restype = Z
+    lib.ddtree_step_args_size.argtypes = []
+    lib.ddtree_step_create.restype = I
+    lib.ddtree_step_create.argtypes = [ctypes.POINTER(StepArgs), ctypes.POINTER(P)]
+    lib.ddtree_step_launch.restype = I
+    lib.ddtree_step_launch.argtypes = [P, P]
+    lib.ddtree_step_destroy.restype = None
+    lib.ddtree_step_destroy.argtypes = [P]
     lib.ddtree_build.restype = I
     lib.ddtree_build.argtypes = [P] * 4 + [I] * 4 + [P] * 10 + [P, P]
     lib.tree_verify_attn.restype = I
@@ -73,6 +84,22 @@ def load_library(path: Optional[str] = None):
     if path is None:
         _lib = lib
     return lib
+
+
+class StepArgs(ctypes.Structure):
+    """Mirror of ``ddtree_step_args`` (include/ddtree.h), field for field."""
+    _fields_ = (
+        [(n, ctypes.c_int) for n in ("B", "D", "K", "budget", "V", "Hq", "Hkv", "Dh", "num_pages",
+                                     "page_size", "max_pages")]
+        + [("scale", ctypes.c_float), ("walk", ctypes.c_int), ("philox_offset", ctypes.c_uint64)]
+        + [(n, ctypes.c_void_p) for n in ("topk_logp", "topk_tok", "root_tok", "ctx_len", "q", "k_tree",
+                                          "v_tree", "k_cache", "v_cache", "page_table", "logits",
+                                          "temperature", "seed", "parent", "depth", "token", "rank",
+                                          "pos", "score", "first_child", "next_sibling", "vis",
+                                          "n_nodes", "attn_out", "lse", "workspace")]
+        + [("workspace_bytes", ctypes.c_size_t)]
+        + [(n, ctypes.c_void_p) for n in ("accept_len", "out_tokens", "out_nodes", "bonus",
+                                          "new_ctx_len", "dev_status")])
 
 
 def _check(status: int, where: str):
@@ -248,6 +275,34 @@ def ddtree_accept_greedy(logits: torch.Tensor, tree: TreeBuffers, D: int, out=No
     return o
 
 
+def ddtree_commit_kv(k_tree: torch.Tensor, v_tree: torch.Tensor, accept: dict,
+                     ctx_len: torch.Tensor, page_table: torch.Tensor, k_cache: torch.Tensor,
+                     v_cache: torch.Tensor, new_ctx_len: Optional[torch.Tensor] = None,
+                     dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Append the committed path's K/V to the paged cache (see ``ddtree_commit_kv`` in
+    include/ddtree.h). ``accept`` is a walk's output dict; ``new_ctx_len`` may be
+    ``ctx_len`` itself (in-place advance). Returns ``new_ctx_len``."""
+    lib = load_library()
+    B, N, Hkv, Dh = k_tree.shape
+    D = accept["out_nodes"].shape[1] - 1
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    max_pages = page_table.shape[1]
+    if new_ctx_len is None:
+        new_ctx_len = torch.empty_like(ctx_len)
+    st = lib.ddtree_commit_kv(
+        _ptr(k_tree, torch.bfloat16, "k_tree", (B, N, Hkv, Dh)),
+        _ptr(v_tree, torch.bfloat16, "v_tree", (B, N, Hkv, Dh)),
+        _ptr(accept["out_nodes"], torch.int32, "out_nodes", (B, D + 1)),
+        _ptr(accept["accept_len"], torch.int32, "accept_len", (B,)), B, N, D, Hkv, Dh,
+        _ptr(k_cache, torch.bfloat16, "k_cache", (num_pages, page_size, Hkv, Dh)),
+        _ptr(v_cache, torch.bfloat16, "v_cache", (num_pages, page_size, Hkv, Dh)),
+        num_pages, page_size, _ptr(page_table, torch.int32, "page_table", (B, max_pages)), max_pages,
+        _ptr(ctx_len, torch.int32, "ctx_len", (B,)), _ptr(new_ctx_len, torch.int32, "new_ctx_len", (B,)),
+        _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
+    _check(st, "ddtree_commit_kv")
+    return new_ctx_len
+
+
 def ddtree_accept_sample(logits: torch.Tensor, tree: TreeBuffers, D: int,
                          temperature: torch.Tensor, seed: torch.Tensor, philox_offset: int,
                          out=None, dev_status: Optional[torch.Tensor] = None, stream=None):
@@ -310,3 +365,86 @@ def tree_verify_attn_noalloc(q: torch.Tensor, k_tree: torch.Tensor, v_tree: torc
             _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
     _check(st, "tree_verify_attn_noalloc")
     return out
+
+
+class VerifyStep:
+    """The verify step (build -> attention -> walk -> commit) recorded by the
+    library as one CUDA graph (``ddtree_step_*`` in include/ddtree.h).
+
+    Every array is fixed at construction; ``launch()`` replays the graph on a
+    stream and reads the arrays' current contents. Outputs not given are
+    allocated here: ``tree`` (TreeBuffers), ``attn_out``, ``accept`` (walk
+    dict). With ``new_ctx_len=None`` each launch advances ``ctx_len`` in place.
+    The object keeps references to all tensors for the graph's lifetime.
+    """
+
+    def __init__(self, *, topk_logp, topk_tok, root_tok, ctx_len, q, k_tree, v_tree, k_cache, v_cache,
+                 page_table, logits, budget: int, scale: float, walk: str = "greedy",
+                 temperature=None, seed=None, philox_offset: int = 0, new_ctx_len=None,
+                 dev_status=None, lse=None):
+        lib = load_library()
+        B, D, K = topk_logp.shape
+        N = budget + 1
+        _, _, Hq, Dh = q.shape
+        num_pages, page_size, Hkv, _ = k_cache.shape
+        max_pages = page_table.shape[1]
+        V = logits.shape[2]
+        dev = q.device
+        if walk not in ("greedy", "sampled"):
+            raise ValueError("walk must be 'greedy' or 'sampled'")
+        self.tree = TreeBuffers(B, N, dev)
+        self.attn_out = torch.empty((B, N, Hq, Dh), dtype=torch.bfloat16, device=dev)
+        self.accept = _walk_outputs(B, D, dev, None)
+        need = tree_verify_attn_workspace_size(B, N, Hq, Hkv, Dh, max_pages * page_size)
+        self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self._keep = [topk_logp, topk_tok, root_tok, ctx_len, q, k_tree, v_tree, k_cache, v_cache,
+                      page_table, logits, temperature, seed, new_ctx_len, dev_status, lse]
+        a = StepArgs()
+        a.B, a.D, a.K, a.budget, a.V, a.Hq, a.Hkv, a.Dh = B, D, K, budget, V, Hq, Hkv, Dh
+        a.num_pages, a.page_size, a.max_pages = num_pages, page_size, max_pages
+        a.scale, a.walk, a.philox_offset = scale, (0 if walk == "greedy" else 1), philox_offset
+        a.topk_logp = _ptr(topk_logp, torch.float32, "topk_logp", (B, D, K))
+        a.topk_tok = _ptr(topk_tok, torch.int32, "topk_tok", (B, D, K))
+        a.root_tok = _ptr(root_tok, torch.int32, "root_tok", (B,))
+        a.ctx_len = _ptr(ctx_len, torch.int32, "ctx_len", (B,))
+        a.q = _ptr(q, torch.bfloat16, "q", (B, N, Hq, Dh))
+        a.k_tree = _ptr(k_tree, torch.bfloat16, "k_tree", (B, N, Hkv, Dh))
+        a.v_tree = _ptr(v_tree, torch.bfloat16, "v_tree", (B, N, Hkv, Dh))
+        a.k_cache = _ptr(k_cache, torch.bfloat16, "k_cache", (num_pages, page_size, Hkv, Dh))
+        a.v_cache = _ptr(v_cache, torch.bfloat16, "v_cache", (num_pages, page_size, Hkv, Dh))
+        a.page_table = _ptr(page_table, torch.int32, "page_table", (B, max_pages))
+        a.logits = _ptr(logits, torch.float32, "logits", (B, N, V))
+        a.temperature = _ptr(temperature, torch.float32, "temperature", (B,))
+        a.seed = _ptr(seed, torch.int64, "seed", (B,))
+        t = self.tree
+        a.parent, a.depth, a.token, a.rank, a.pos = (x.data_ptr() for x in (t.parent, t.depth, t.token,
+                                                                             t.rank, t.pos))
+        a.score, a.first_child, a.next_sibling = t.score.data_ptr(), t.first_child.data_ptr(), \
+            t.next_sibling.data_ptr()
+        a.vis, a.n_nodes = t.vis.data_ptr(), t.n_nodes.data_ptr()
+        a.attn_out = self.attn_out.data_ptr()
+        a.lse = _ptr(lse, torch.float32, "lse", (B, N, Hq))
+        a.workspace, a.workspace_bytes = self.workspace.data_ptr(), self.workspace.numel()
+        o = self.accept
+        a.accept_len, a.out_tokens = o["accept_len"].data_ptr(), o["out_tokens"].data_ptr()
+        a.out_nodes, a.bonus = o["out_nodes"].data_ptr(), o["bonus"].data_ptr()
+        a.new_ctx_len = _ptr(new_ctx_len, torch.int32, "new_ctx_len", (B,))
+        a.dev_status = _ptr(dev_status, torch.int32, "dev_status", (1,))
+        self._args = a
+        handle = ctypes.c_void_p()
+        _check(lib.ddtree_step_create(ctypes.byref(a), ctypes.byref(handle)), "ddtree_step_create")
+        self._handle = handle
+
+    def launch(self, stream=None):
+        _check(load_library().ddtree_step_launch(self._handle, _stream(stream)), "ddtree_step_launch")
+
+    def close(self):
+        if getattr(self, "_handle", None):
+            load_library().ddtree_step_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -19,16 +19,20 @@ cudaError_t launch_accept_sample(const float*, int, const int32_t*, const int32_
                                  const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*,
                                  int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_draft_topk(const float*, int, int, int, int, float*, int32_t*, cudaStream_t);
-
-namespace {
+cudaError_t launch_commit_kv(const ddtree_bf16*, const ddtree_bf16*, const int32_t*, const int32_t*, int,
+                             int, int, int, int, ddtree_bf16*, ddtree_bf16*, int, int, const int32_t*,
+                             int, const int32_t*, int32_t*, int32_t*, cudaStream_t);
 
 thread_local char g_last_error[256] = "";
 
+// records the error text for ddtree_last_error(); shared with the step graph
 int cuda_fail(cudaError_t e) {
     std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
                   cudaGetErrorString(e));
     return DDT_ECUDA;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -222,6 +226,28 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                                          N, D, temperature, seed, philox_offset, accept_len,
                                          out_tokens, out_nodes, bonus, dev_status,
                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+int ddtree_commit_kv(const ddtree_bf16* k_tree, const ddtree_bf16* v_tree, const int32_t* out_nodes,
+                     const int32_t* accept_len, int B, int N, int D, int Hkv, int Dh,
+                     ddtree_bf16* k_cache, ddtree_bf16* v_cache, int num_pages, int page_size,
+                     const int32_t* page_table, int max_pages, const int32_t* ctx_len,
+                     int32_t* new_ctx_len, int32_t* dev_status, void* stream) {
+    if (B < 0 || Hkv < 1 || Dh < 1 || page_size < 1 || max_pages < 1 || num_pages < 1)
+        return DDT_EINVAL;
+    if (N < 1 || N > DDT_MAX_NODES || D < 1 || D > DDT_MAX_DEPTH ||
+        (static_cast<long long>(Hkv) * Dh) % 8 != 0 || static_cast<long long>(Hkv) * Dh > (1 << 20))
+        return DDT_ESHAPE;
+    if (B == 0) return DDT_OK;
+    if (!k_tree || !v_tree || !out_nodes || !accept_len || !k_cache || !v_cache || !page_table ||
+        !ctx_len || !new_ctx_len)
+        return DDT_EINVAL;
+    if (!aligned16(k_tree) || !aligned16(v_tree) || !aligned16(k_cache) || !aligned16(v_cache))
+        return DDT_EINVAL;
+    cudaError_t e = launch_commit_kv(k_tree, v_tree, out_nodes, accept_len, B, N, D, Hkv, Dh, k_cache,
+                                     v_cache, num_pages, page_size, page_table, max_pages, ctx_len,
+                                     new_ctx_len, dev_status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
 
