@@ -10,4 +10,5 @@ from .ddtree_oracle import (Tree, Accept, draft_topk, build_tree, child_lists,
                             tree_verify_attention, attention_row, argmax_lowest,
                             accept_greedy, accept_sample, philox4x32_10,
                             philox4x32_10_np, draw_words, to_uniform, bf16_to_f64,
-                            children, gather_context, commit_kv)
+                            children, gather_context, commit_kv,
+                            accept_sample_ratio)

@@ -622,3 +622,111 @@ def commit_kv(k_tree, v_tree, out_nodes, accept_len, ctx_len, page_table, k_cach
             vc[page, slot] = v_tree[b, node]
         new_ctx[b] = int(ctx_len[b]) + a + 1
     return kc, vc, new_ctx
+
+
+# ----------------------------------------------------------------------------
+# draft-ratio temperature walk (the min(1, q/p) rule with the draft softmax)
+# ----------------------------------------------------------------------------
+
+def accept_sample_ratio(logits: np.ndarray, draft_logits: np.ndarray, tree: Tree, D: int,
+                        temperature: np.ndarray, seed: np.ndarray, offset: int) -> Accept:
+    """Tree verification at temperature T with the draft-ratio rule.
+
+    [Arch] §"Section 3: Temperature Support": linear case, accept draft token
+    t with probability min(1, p_target(t) / p_draft(t)), else resample from
+    the residual; tree case, reject-sample each node's children against their
+    draft probabilities and, once they are all rejected, draw the bonus from
+    the residual and stop. [Verify] §"The Knowledge Required …" item 3
+    (accept with min(1, q/p); after a rejection the target distribution is
+    renormalised over what remains) and §"Path B" (softmax only at the nodes
+    visited). [Arch] §"Mistakes and Incorrect Assumptions" (the rule needs
+    the draft's full distribution, not only its top-k): this walk takes the
+    draft logits.
+
+    Readings (pages silent):
+    * p = softmax(draft_logits[b, d] / T) is the draft distribution the
+      children of a depth-d node were taken from (the row whose top-k they
+      are); q = softmax(logits[b, u] / T) at node u; one T for both.
+    * Children are tested in rank order against a residual r that starts at
+      q: child j (token x_j) is accepted when U_j * p(x_j) < r(x_j), i.e.
+      with probability min(1, r(x_j) / p(x_j)); after a rejection
+      r <- max(r - p, 0) / sum(max(r - p, 0)) (the SpecInfer-style update, so
+      that candidates drawn independently from p emit tokens distributed as
+      q). If a rejection leaves r without mass, no further child is tested
+      and the bonus is drawn from q.
+    * The bonus is drawn from the final r (r = q at a node without children,
+      including every depth-D node) by Gumbel-max over the tokens with
+      r > 0; the linear chain is the top-k-1 tree.
+
+    Randomness as ``accept_sample``: U(node u, slot j) from the accept purpose,
+    word 0; Gumbel noise of vocab entry v from the Gumbel purpose at index
+    v >> 2, word v & 3. ``margin[b]`` is the smallest decision margin on the
+    path: |U_j - r(x_j)/p(x_j)| for each child test and the gap between the
+    two best perturbed scores for the bonus.
+    """
+    B, N, V = logits.shape
+    acc = np.zeros(B, np.int32)
+    toks = np.full((B, D + 1), -1, np.int32)
+    nodes = np.full((B, D + 1), -1, np.int32)
+    bonus = np.zeros(B, np.int32)
+    margin = np.full(B, np.inf)
+    vidx = np.arange(V, dtype=np.uint64)
+
+    def softmax_t(row, T):
+        z = np.asarray(row, dtype=np.float64) / T
+        e = np.exp(z - z.max())
+        return e / e.sum()
+
+    for b in range(B):
+        T = float(temperature[b])
+        if not T > 0.0:
+            raise ValueError("temperature must be > 0")
+        sd = int(seed[b])
+        u = 0
+        path = []
+        while True:
+            q = softmax_t(logits[b, u], T)
+            r = q
+            kids = children(tree, b, u) if len(path) < D else []
+            chosen = -1
+            if kids:
+                p = softmax_t(draft_logits[b, len(path)], T)
+                for j, c in enumerate(kids):
+                    x = int(tree.token[b, c])
+                    uj = float(to_uniform(draw_words(sd, offset, PURPOSE_ACCEPT, u, j)[0]))
+                    if p[x] > 0.0:
+                        margin[b] = min(margin[b], abs(uj - r[x] / p[x]))
+                    if uj * p[x] < r[x]:
+                        chosen = c
+                        break
+                    res = np.maximum(r - p, 0.0)
+                    mass = res.sum()
+                    if not mass > 0.0:   # nothing left to renormalise: the bonus comes from q
+                        r = q
+                        break
+                    r = res / mass
+            if chosen != -1:
+                path.append(chosen)
+                u = chosen
+                continue
+            words = draw_words(sd, offset, PURPOSE_GUMBEL, u, vidx >> np.uint64(2))
+            stacked = np.stack(words, axis=0)                   # [4, V]
+            w = stacked[(vidx & np.uint64(3)).astype(np.int64), np.arange(V)]
+            g = -np.log(-np.log(to_uniform(w)))
+            cand = np.nonzero(r > 0.0)[0]
+            if cand.size == 0:
+                bonus[b] = -1
+            else:
+                pert = np.log(r[cand]) + g[cand]
+                bonus[b] = int(cand[np.argmax(pert)])
+                if cand.size >= 2:
+                    top2 = np.partition(pert, -2)[-2:]
+                    margin[b] = min(margin[b], float(top2[1] - top2[0]))
+            break
+        acc[b] = len(path)
+        nodes[b, 0] = 0
+        for k, c in enumerate(path):
+            toks[b, k] = tree.token[b, c]
+            nodes[b, k + 1] = c
+        toks[b, len(path)] = bonus[b]
+    return Accept(acc, toks, nodes, bonus, margin)

@@ -655,3 +655,103 @@ def test_commit_of_a_chain_is_the_linear_dflash_commit():
     assert new_ctx.tolist() == [9]
     seq = O.gather_context(kc, table, 0, 9, 4)
     assert np.array_equal(seq[5:9], k_tree[0, 0:4])
+
+
+# ---------------------------------------------------------------------------
+# draft-ratio temperature walk
+# ---------------------------------------------------------------------------
+
+def _star_tree(child_tokens):
+    """Root 0 with children 1..k (depth 1, leaves) carrying the given tokens in rank order."""
+    k = len(child_tokens)
+    lp = -np.arange(1, k + 1, dtype=np.float32)[None, None, :] * 0.1
+    tok = np.asarray(child_tokens, np.int32)[None, None, :]
+    return O.build_tree(lp, tok, np.array([0]), np.array([0]), k)
+
+
+def _softmax64(x, T):
+    z = np.asarray(x, np.float64) / T
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+@pytest.mark.parametrize("k", [1, 3])
+def test_ratio_iid_candidates_emit_the_target_distribution(k):
+    """Chi-square: with the k candidates drawn independently from the draft
+    distribution p, the first emitted token follows q = softmax(target / T)
+    (k = 1: the speculative-sampling theorem of the linear chain; k > 1: the
+    multi-candidate residual update)."""
+    from scipy.stats import chisquare
+    rng = np.random.default_rng(40 + k)
+    V, T, n = 6, 0.9, 6000
+    logits = (rng.standard_normal((1, k + 1, V)) * 1.2).astype(np.float32)
+    draft = (rng.standard_normal((1, 1, V)) * 1.2).astype(np.float32)
+    p = _softmax64(draft[0, 0], T)
+    q = _softmax64(logits[0, 0], T)
+    counts = np.zeros(V, np.int64)
+    draws = rng.choice(V, size=(n, k), p=p)
+    for s in range(n):
+        t = _star_tree(draws[s])
+        r = O.accept_sample_ratio(logits, draft, t, 1, np.array([T], np.float32),
+                                  np.array([5_000_000 + s], np.uint64), 3)
+        counts[r.out_tokens[0, 0]] += 1
+    assert chisquare(counts, q * n).pvalue > 0.001 / 2
+
+
+def test_ratio_single_child_is_accepted_with_min_one_q_over_p():
+    """One fixed child x: accepted with probability min(1, q(x)/p(x)) (binomial, 4 sigma)."""
+    rng = np.random.default_rng(7)
+    V, T, n = 8, 0.7, 4000
+    logits = (rng.standard_normal((1, 2, V)) * 1.5).astype(np.float32)
+    draft = (rng.standard_normal((1, 1, V)) * 1.5).astype(np.float32)
+    p = _softmax64(draft[0, 0], T)
+    q = _softmax64(logits[0, 0], T)
+    for x in (int(np.argmax(p)), int(np.argmax(q))):
+        t = _star_tree([x])
+        hits = sum(int(O.accept_sample_ratio(logits, draft, t, 1, np.array([T], np.float32),
+                                             np.array([s], np.uint64), 11).accept_len[0])
+                   for s in range(n))
+        a = min(1.0, q[x] / p[x])
+        assert abs(hits / n - a) <= 4 * math.sqrt(a * (1 - a) / n) + 1e-9
+
+
+def test_ratio_equal_draft_and_target_accept_every_level():
+    # p == q at every node: r(x)/p(x) = 1 > U, so the walk takes the top child
+    # at each level and reaches depth D
+    rng = np.random.default_rng(3)
+    B, D, V = 3, 5, 20
+    draft = (rng.standard_normal((B, D, V)) * 2).astype(np.float32)
+    lp, tok = O.draft_topk(draft, 2)
+    tree = O.build_tree(lp, tok, np.zeros(B, np.int32), np.zeros(B, np.int32), 12)
+    logits = np.zeros((B, 13, V), np.float32)
+    for b in range(B):
+        for u in range(int(tree.n_nodes[b])):
+            d = int(tree.depth[b, u])
+            logits[b, u] = draft[b, d] if d < D else rng.standard_normal(V)
+    for s in range(20):
+        r = O.accept_sample_ratio(logits, draft, tree, D, np.full(B, 0.8, np.float32),
+                                  np.arange(B, dtype=np.uint64) + 100 * s, 0)
+        for b in range(B):
+            path = r.out_nodes[b, 1:r.accept_len[b] + 1]
+            assert all(int(tree.rank[b, c]) == 0 for c in path)   # always the first child
+            last = int(r.out_nodes[b, r.accept_len[b]])
+            assert int(tree.first_child[b, last]) == -1           # stopped at a leaf
+
+
+def test_ratio_leaf_bonus_equals_the_renormalising_walk():
+    # a node without children draws its bonus from q in both walks, from the
+    # same Gumbel noise: the two oracles agree exactly (accept_sample is pinned
+    # by its own chi-square tests)
+    rng = np.random.default_rng(12)
+    B, V = 4, 50
+    lp = np.zeros((B, 1, 1), np.float32)
+    tok = np.zeros((B, 1, 1), np.int32)
+    tree = O.build_tree(lp, tok, np.zeros(B, np.int32), np.zeros(B, np.int32), 0)   # root only
+    logits = (rng.standard_normal((B, 1, V)) * 2).astype(np.float32)
+    draft = (rng.standard_normal((B, 1, V)) * 2).astype(np.float32)
+    for s in range(10):
+        T = np.full(B, 0.6 + 0.1 * s, np.float32)
+        seed = np.arange(B, dtype=np.uint64) + 1000 * s
+        a = O.accept_sample(logits, tree, 1, T, seed, 5)
+        r = O.accept_sample_ratio(logits, draft, tree, 1, T, seed, 5)
+        assert np.array_equal(a.bonus, r.bonus) and (r.accept_len == 0).all()
