@@ -5,9 +5,10 @@ One step = the whole hot path over one batch: ddtree_build -> tree_verify_attn
 same tree at T = 0.7, as a server would for the temperature requests of a
 batch; the two walks are independent and run concurrently on two streams).
 The step's input, the per-depth top-k, is made once by ddtree_draft_topk
-from the draft logits; that call, ddtree_commit_kv and the library's own
-step graph (build, attention, greedy walk, commit: ddtree_step_*) are timed
-on their own (`per_call_us`).
+from the draft logits; that call, the draft-ratio walk
+(ddtree_accept_sample_ratio), ddtree_commit_kv and the library's own step
+graph (build, attention, greedy walk, commit: ddtree_step_*) are timed on
+their own (`per_call_us`).
 
 The default workload is the batched serving case: 16 requests with contexts
 uniform in [1024, 16384] tokens (paged, page 64, shuffled pages), 64 query /
@@ -347,6 +348,7 @@ def run_native(args):
               out_nodes=torch.empty((w.B, w.D + 1), dtype=torch.int32, device=device),
               bonus=torch.empty(w.B, dtype=torch.int32, device=device))
     so = {k: torch.empty_like(t) for k, t in go.items()}
+    ro = {k: torch.empty_like(t) for k, t in go.items()}
     scale = 1.0 / math.sqrt(w.Dh)
 
     walk_stream = torch.cuda.Stream(device)
@@ -405,6 +407,8 @@ def run_native(args):
         "ddtree_accept_greedy": lambda: dd.ddtree_accept_greedy(logits, tree, w.D, out=go, dev_status=status),
         "ddtree_accept_sample": lambda: dd.ddtree_accept_sample(logits, tree, w.D, temp, seed, 0, out=so,
                                                                 dev_status=status),
+        "ddtree_accept_sample_ratio": lambda: dd.ddtree_accept_sample_ratio(logits, dl_d, tree, w.D, temp, seed,
+                                                                            0, out=ro, dev_status=status),
     }
     call_graphs = {n: graph_of(f, 10) for n, f in calls.items()}
     torch.cuda.synchronize()

@@ -12,6 +12,7 @@
  *   ddtree_accept_greedy  longest root path matching the target argmax + bonus
  *   ddtree_accept_sample  the same at temperature, by recursive rejection
  *                         sampling over siblings + a bonus from the residual
+ *                         (ddtree_accept_sample_ratio: the draft-ratio rule)
  *
  * and ddtree_commit_kv appends the committed path's K/V to the paged cache;
  * ddtree_step_* records build -> attention -> walk -> commit as one graph.
@@ -284,6 +285,41 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                          int32_t* dev_status, void* stream);
 
 /*
+ * ddtree_accept_sample_ratio - the temperature walk with the draft-ratio rule.
+ *
+ * [Arch] Section 3 (linear case: accept draft token t with probability
+ * min(1, p_target(t) / p_draft(t)), else resample from the residual; tree
+ * case: reject-sample the children, bonus from the residual); [Verify] The
+ * Knowledge Required, item 3; [Arch] Mistakes and Incorrect Assumptions (the
+ * rule needs the draft's full distribution): this call takes the draft
+ * logits. At node u (depth d): q = softmax(logits[b, u] / T),
+ * p = softmax(draft_logits[b, d] / T) (the row the children were taken from).
+ * Children are tested in rank order against a residual r that starts at q:
+ * child j (token x) is accepted when U_j * p(x) < r(x), i.e. with probability
+ * min(1, r(x) / p(x)); after a rejection r <- normalise(max(r - p, 0)). Once
+ * every child is rejected (or at a node without children) the bonus is drawn
+ * from r by Gumbel-max; if a rejection leaves r without mass, from q. With
+ * candidates drawn independently from p the emitted tokens follow q; a
+ * top-k-1 tree is linear speculative sampling. Cost: one pass over the
+ * target and draft rows per visited node, one more per rejection.
+ *
+ * Inputs and outputs as ddtree_accept_sample, plus
+ *   draft_logits  fp32 [B, D, V]   as given to ddtree_draft_topk
+ * Randomness: the counters of ddtree_accept_sample (child test: purpose 0,
+ * node u, slot j, word 0; Gumbel noise of token v: purpose 1, node u, index
+ * v >> 2, word v & 3). A child whose token is outside [0, V) sets
+ * DDT_DEV_BAD_TOKEN and is skipped. Device errors as ddtree_accept_sample.
+ */
+int ddtree_accept_sample_ratio(const float* logits, const float* draft_logits, int V,
+                               const int32_t* token, const int32_t* first_child,
+                               const int32_t* next_sibling, const int32_t* n_nodes,
+                               int B, int N, int D, const float* temperature,
+                               const uint64_t* seed, uint64_t philox_offset,
+                               int32_t* accept_len, int32_t* out_tokens,
+                               int32_t* out_nodes, int32_t* bonus,
+                               int32_t* dev_status, void* stream);
+
+/*
  * ddtree_commit_kv - append the committed path's K/V to the paged cache.
  *
  * [Arch] Section 1, step 5: only the single longest verified path is
@@ -348,7 +384,7 @@ typedef struct ddtree_step_args {
     /* sizes */
     int B, D, K, budget, V, Hq, Hkv, Dh, num_pages, page_size, max_pages;
     float scale;                 /* attention scale                          */
-    int walk;                    /* 0: greedy walk, 1: sampled walk          */
+    int walk;                    /* 0 greedy, 1 sampled, 2 draft-ratio walk  */
     uint64_t philox_offset;      /* sampled walk only                        */
     /* inputs (device) */
     const float* topk_logp;      /* [B, D, K]        ddtree_build            */
@@ -365,6 +401,7 @@ typedef struct ddtree_step_args {
     const float* logits;         /* [B, N, V]        the walk                */
     const float* temperature;    /* [B]              sampled walk only       */
     const uint64_t* seed;        /* [B]              sampled walk only       */
+    const float* draft_logits;   /* [B, D, V]        draft-ratio walk only   */
     /* tree (ddtree_build outputs) */
     int32_t* parent; int32_t* depth; int32_t* token; int32_t* rank; int32_t* pos;
     double* score; int32_t* first_child; int32_t* next_sibling;

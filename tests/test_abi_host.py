@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_four_calls():
     names = declared_functions()
-    for n in ("ddtree_draft_topk", "ddtree_commit_kv", "ddtree_build", "tree_verify_attn", "ddtree_accept_greedy", "ddtree_accept_sample"):
+    for n in ("ddtree_draft_topk", "ddtree_commit_kv", "ddtree_accept_sample_ratio", "ddtree_build", "tree_verify_attn", "ddtree_accept_greedy", "ddtree_accept_sample"):
         assert n in names
 
 
@@ -170,6 +170,23 @@ def test_walks_reject_bad_arguments(lib, kw, code):
     assert lib.ddtree_accept_sample(*walk_args(sample=True, **kw)) == code
 
 
+def ratio_args(draft=FAKE, **kw):
+    a = walk_args(sample=True, **kw)
+    return a[:1] + [draft] + a[1:]
+
+
+@pytest.mark.parametrize("kw,code", [(dict(V=0), -1), (dict(N=200), -2), (dict(D=0), -2),
+                                     (dict(D=65), -2), (dict(B=-1), -1), (dict(logits=0), -1),
+                                     (dict(token=0), -1), (dict(bonus=0), -1), (dict(draft=0), -1),
+                                     (dict(temp=0), -1), (dict(seed=0), -1), (dict(offset=1 << 56), -1)])
+def test_ratio_walk_rejects_bad_arguments(lib, kw, code):
+    assert lib.ddtree_accept_sample_ratio(*ratio_args(**kw)) == code
+
+
+def test_ratio_walk_empty_batch_is_a_noop(lib):
+    assert lib.ddtree_accept_sample_ratio(*ratio_args(B=0, logits=0, draft=0)) == 0
+
+
 def test_sample_rejects_missing_rng_inputs_and_large_offset(lib):
     assert lib.ddtree_accept_sample(*walk_args(sample=True, temp=0)) == -1
     assert lib.ddtree_accept_sample(*walk_args(sample=True, seed=0)) == -1
@@ -184,9 +201,9 @@ def test_step_args_mirror_matches_the_c_struct(lib):
 def test_step_create_rejects_before_any_cuda_call(lib):
     import tree_speculative_decoding_ddtree_gb300 as dd
     a = dd.StepArgs()
-    a.B, a.walk = 2, 2
+    a.B, a.walk = 2, 3
     h = ctypes.c_void_p()
-    assert lib.ddtree_step_create(ctypes.byref(a), ctypes.byref(h)) == -1   # walk not 0/1
+    assert lib.ddtree_step_create(ctypes.byref(a), ctypes.byref(h)) == -1   # walk not 0, 1, 2
     a.walk, a.B = 0, 0
     assert lib.ddtree_step_create(ctypes.byref(a), ctypes.byref(h)) == -2   # empty batch
     assert lib.ddtree_step_create(None, ctypes.byref(h)) == -1

@@ -21,7 +21,7 @@ __all__ = [
     "DDTreeError", "load_library", "library_path", "ddtree_draft_topk", "ddtree_build", "tree_verify_attn",
     "tree_verify_attn_workspace_size", "ddtree_accept_greedy", "ddtree_accept_sample",
     "TreeBuffers", "alloc_tree", "DEV_ERRORS", "tree_verify_attn_noalloc", "ddtree_commit_kv",
-    "StepArgs", "VerifyStep",
+    "StepArgs", "VerifyStep", "ddtree_accept_sample_ratio",
 ]
 
 DEV_ERRORS = {
@@ -70,6 +70,8 @@ def load_library(path: Optional[str] = None):
     lib.ddtree_step_launch.argtypes = [P, P]
     lib.ddtree_step_destroy.restype = None
     lib.ddtree_step_destroy.argtypes = [P]
+    lib.ddtree_accept_sample_ratio.restype = I
+    lib.ddtree_accept_sample_ratio.argtypes = [P, P, I, P, P, P, P, I, I, I, P, P, U64, P, P, P, P, P, P]
     lib.ddtree_build.restype = I
     lib.ddtree_build.argtypes = [P] * 4 + [I] * 4 + [P] * 10 + [P, P]
     lib.tree_verify_attn.restype = I
@@ -94,7 +96,7 @@ class StepArgs(ctypes.Structure):
         + [("scale", ctypes.c_float), ("walk", ctypes.c_int), ("philox_offset", ctypes.c_uint64)]
         + [(n, ctypes.c_void_p) for n in ("topk_logp", "topk_tok", "root_tok", "ctx_len", "q", "k_tree",
                                           "v_tree", "k_cache", "v_cache", "page_table", "logits",
-                                          "temperature", "seed", "parent", "depth", "token", "rank",
+                                          "temperature", "seed", "draft_logits", "parent", "depth", "token", "rank",
                                           "pos", "score", "first_child", "next_sibling", "vis",
                                           "n_nodes", "attn_out", "lse", "workspace")]
         + [("workspace_bytes", ctypes.c_size_t)]
@@ -275,6 +277,33 @@ def ddtree_accept_greedy(logits: torch.Tensor, tree: TreeBuffers, D: int, out=No
     return o
 
 
+def ddtree_accept_sample_ratio(logits: torch.Tensor, draft_logits: torch.Tensor, tree: TreeBuffers,
+                               D: int, temperature: torch.Tensor, seed: torch.Tensor, philox_offset: int,
+                               out=None, dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Temperature walk with the draft-ratio rule (see ``ddtree_accept_sample_ratio`` in
+    include/ddtree.h). ``draft_logits`` fp32 ``[B, D, V]``; ``seed`` int64 ``[B]``
+    holding the uint64 seeds."""
+    lib = load_library()
+    B, N, V = logits.shape
+    o = _walk_outputs(B, D, logits.device, out)
+    st = lib.ddtree_accept_sample_ratio(
+        _ptr(logits, torch.float32, "logits", (B, N, V)),
+        _ptr(draft_logits, torch.float32, "draft_logits", (B, D, V)), V,
+        _ptr(tree.token, torch.int32, "token", (B, N)),
+        _ptr(tree.first_child, torch.int32, "first_child", (B, N)),
+        _ptr(tree.next_sibling, torch.int32, "next_sibling", (B, N)),
+        _ptr(tree.n_nodes, torch.int32, "n_nodes", (B,)), B, N, D,
+        _ptr(temperature, torch.float32, "temperature", (B,)),
+        _ptr(seed, torch.int64, "seed", (B,)), philox_offset,
+        _ptr(o["accept_len"], torch.int32, "accept_len", (B,)),
+        _ptr(o["out_tokens"], torch.int32, "out_tokens", (B, D + 1)),
+        _ptr(o["out_nodes"], torch.int32, "out_nodes", (B, D + 1)),
+        _ptr(o["bonus"], torch.int32, "bonus", (B,)),
+        _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
+    _check(st, "ddtree_accept_sample_ratio")
+    return o
+
+
 def ddtree_commit_kv(k_tree: torch.Tensor, v_tree: torch.Tensor, accept: dict,
                      ctx_len: torch.Tensor, page_table: torch.Tensor, k_cache: torch.Tensor,
                      v_cache: torch.Tensor, new_ctx_len: Optional[torch.Tensor] = None,
@@ -381,7 +410,7 @@ class VerifyStep:
     def __init__(self, *, topk_logp, topk_tok, root_tok, ctx_len, q, k_tree, v_tree, k_cache, v_cache,
                  page_table, logits, budget: int, scale: float, walk: str = "greedy",
                  temperature=None, seed=None, philox_offset: int = 0, new_ctx_len=None,
-                 dev_status=None, lse=None):
+                 dev_status=None, lse=None, draft_logits=None):
         lib = load_library()
         B, D, K = topk_logp.shape
         N = budget + 1
@@ -390,19 +419,21 @@ class VerifyStep:
         max_pages = page_table.shape[1]
         V = logits.shape[2]
         dev = q.device
-        if walk not in ("greedy", "sampled"):
-            raise ValueError("walk must be 'greedy' or 'sampled'")
+        walks = {"greedy": 0, "sampled": 1, "ratio": 2}
+        if walk not in walks:
+            raise ValueError("walk must be 'greedy', 'sampled' or 'ratio'")
         self.tree = TreeBuffers(B, N, dev)
         self.attn_out = torch.empty((B, N, Hq, Dh), dtype=torch.bfloat16, device=dev)
         self.accept = _walk_outputs(B, D, dev, None)
         need = tree_verify_attn_workspace_size(B, N, Hq, Hkv, Dh, max_pages * page_size)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
         self._keep = [topk_logp, topk_tok, root_tok, ctx_len, q, k_tree, v_tree, k_cache, v_cache,
-                      page_table, logits, temperature, seed, new_ctx_len, dev_status, lse]
+                      page_table, logits, temperature, seed, new_ctx_len, dev_status, lse,
+                      draft_logits]
         a = StepArgs()
         a.B, a.D, a.K, a.budget, a.V, a.Hq, a.Hkv, a.Dh = B, D, K, budget, V, Hq, Hkv, Dh
         a.num_pages, a.page_size, a.max_pages = num_pages, page_size, max_pages
-        a.scale, a.walk, a.philox_offset = scale, (0 if walk == "greedy" else 1), philox_offset
+        a.scale, a.walk, a.philox_offset = scale, walks[walk], philox_offset
         a.topk_logp = _ptr(topk_logp, torch.float32, "topk_logp", (B, D, K))
         a.topk_tok = _ptr(topk_tok, torch.int32, "topk_tok", (B, D, K))
         a.root_tok = _ptr(root_tok, torch.int32, "root_tok", (B,))
@@ -416,6 +447,7 @@ class VerifyStep:
         a.logits = _ptr(logits, torch.float32, "logits", (B, N, V))
         a.temperature = _ptr(temperature, torch.float32, "temperature", (B,))
         a.seed = _ptr(seed, torch.int64, "seed", (B,))
+        a.draft_logits = _ptr(draft_logits, torch.float32, "draft_logits", (B, D, V))
         t = self.tree
         a.parent, a.depth, a.token, a.rank, a.pos = (x.data_ptr() for x in (t.parent, t.depth, t.token,
                                                                              t.rank, t.pos))

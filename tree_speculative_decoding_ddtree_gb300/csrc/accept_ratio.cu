@@ -1,0 +1,363 @@
+// ddtree_accept_sample_ratio: the temperature walk with the draft-ratio rule.
+//
+// Method: "The Architecture of Speculative Decoding: Dissecting DDTree's
+// Tree-Parallel Evaluation Strategy", Section 3 (linear case: accept draft
+// token t with probability min(1, p_target(t) / p_draft(t)), else resample
+// from the residual; tree case: reject-sample the children, bonus from the
+// residual) and "The Architecture of Speculative Verification: Implementing
+// Temperature-Aware Tree Sampling for DDTree", The Knowledge Required, item 3.
+// p = softmax(draft row d / T) for the children of a depth-d node and
+// q = softmax(target row / T). Children are tested in rank order against a
+// residual r that starts at q; after a rejection r <- normalise(max(r - p, 0)).
+// Written out, r = max(q - c p, 0) / R with c = 0, R = 1 at first and, after
+// each rejection, c <- c + R and R <- sum_v max(q(v) - c p(v), 0): a rejection
+// costs one pass over both rows. Child j (token x) is accepted when
+// U_j * p(x) < r(x). The bonus is the Gumbel-max of log max(q - c p, 0); if
+// the residual has no mass left the bonus is drawn from q.
+//
+// Same layout as the other walks: one 8-CTA cluster per request; every pass
+// over a row is split into the CTAs' slices and combined through distributed
+// shared memory in rank order, so every CTA holds identical values and takes
+// identical decisions; CTA 0 writes the outputs.
+#include "walk.cuh"
+
+namespace ddt {
+
+namespace {
+
+enum ChildState { kAccept = 1, kReject = 2, kSkip = 3 };
+
+// block-wide sum of one float per thread (every thread gets the result)
+DDT_DEVINL float block_sum_f(float v, float* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum_f(v);
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float x = lane < kWalkThreads / 32 ? scratch[lane] : 0.0f;
+        x = warp_sum_f(x);
+        if (lane == 0) scratch[0] = x;
+    }
+    __syncthreads();
+    return scratch[0];
+}
+
+// block-wide (max, sum) merge of one MaxSum per thread; thread 0 gets the result
+DDT_DEVINL MaxSum block_ms(MaxSum ms, float inv_t, float* sm, float* sz) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
+        ms = merge_ms(ms, other, inv_t);
+    }
+    __syncthreads();
+    if (lane == 0) { sm[warp] = ms.m; sz[warp] = ms.z; }
+    __syncthreads();
+    if (warp == 0) {
+        ms.m = lane < kWalkThreads / 32 ? sm[lane] : -INFINITY;
+        ms.z = lane < kWalkThreads / 32 ? sz[lane] : 0.0f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
+            ms = merge_ms(ms, other, inv_t);
+        }
+    }
+    return ms;
+}
+
+DDT_DEVINL void ms_add(MaxSum& ms, float x, float inv_t) {
+    if (x > ms.m) {
+        ms.z = ms.z * expf((ms.m - x) * inv_t) + 1.0f;
+        ms.m = x;
+    } else {
+        ms.z += expf((x - ms.m) * inv_t);
+    }
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWalkThreads)
+accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ draft, int V, bool vec4,
+                    const int32_t* __restrict__ token, const int32_t* __restrict__ first_child,
+                    const int32_t* __restrict__ next_sibling, const int32_t* __restrict__ n_nodes,
+                    int N, int D, const float* __restrict__ temperature,
+                    const uint64_t* __restrict__ seed, uint64_t offset, WalkOut o, int32_t* dev_status) {
+    __shared__ unsigned long long scratch_u[32];
+    __shared__ float scratch_a[32], scratch_b[32];
+    __shared__ float4 part_s[2];                // (max, sum) of the target and the draft row, by round
+    __shared__ float part_r[2];                 // residual mass, by round
+    __shared__ unsigned long long part_g[2];    // Gumbel-max, by round
+    __shared__ TreeRows tr;
+    __shared__ int s_kid_tok[kMaxKids];
+    __shared__ int s_kid_node[kMaxKids];
+    __shared__ float s_kid_l[kMaxKids];         // target logit of the child's token
+    __shared__ float s_kid_d[kMaxKids];         // draft logit of the child's token
+    __shared__ double s_u[kMaxKids];
+    __shared__ float s_mq, s_zq, s_mp, s_zp, s_R;
+    __shared__ unsigned long long s_best;
+    __shared__ int s_nkids, s_state, s_next, s_len;
+    const uint32_t rank = cluster_rank();
+    const bool writer = rank == 0;
+    const int b = static_cast<int>(blockIdx.x) / kCluster;
+    const size_t tb = static_cast<size_t>(b) * N;
+    const Slice sl = row_slice(V, vec4, rank);
+    int32_t* toks = o.out_tokens + static_cast<size_t>(b) * (D + 1);
+    int32_t* nodes = o.out_nodes + static_cast<size_t>(b) * (D + 1);
+    if (writer)
+        for (int k = threadIdx.x; k <= D; k += kWalkThreads) { toks[k] = -1; nodes[k] = -1; }
+    stage_tree(tr, token, first_child, next_sibling, tb, N);
+    int nn = n_nodes[b];
+    if (nn < 1 || nn > N) {
+        if (threadIdx.x == 0 && writer) report(dev_status, DDT_DEV_BAD_TREE);
+        nn = nn < 1 ? 1 : N;
+    }
+    const float T = temperature[b];
+    __syncthreads();
+    if (!(T > 0.0f) || !isfinite(T)) {   // the same decision in every CTA of the cluster
+        if (threadIdx.x == 0 && writer) {
+            report(dev_status, DDT_DEV_BAD_TEMPERATURE);
+            o.accept_len[b] = 0;
+            o.bonus[b] = -1;
+        }
+        return;
+    }
+    const float inv_t = 1.0f / T;
+    const uint64_t sd = seed[b];
+    const uint32_t k0 = static_cast<uint32_t>(sd), k1 = static_cast<uint32_t>(sd >> 32);
+    const uint32_t off_lo = static_cast<uint32_t>(offset);
+    const uint32_t off_hi8 = static_cast<uint32_t>(offset >> 32) << 8;
+    if (threadIdx.x == 0) {
+        s_len = 0;
+        if (writer) nodes[0] = 0;
+    }
+    int round = 0;   // cluster reductions so far: partial slots alternate by its parity
+    int u = 0;
+    for (;;) {
+        const float* row = logits + (tb + u) * static_cast<size_t>(V);
+        if (threadIdx.x == 0) {   // the node's children, in rank order
+            int c = tr.fc[u], j = 0;
+            while (c != -1) {
+                if (c < 1 || c >= nn || j >= kMaxKids) {
+                    if (writer) report(dev_status, DDT_DEV_BAD_TREE);
+                    break;
+                }
+                s_kid_node[j] = c;
+                s_kid_tok[j] = tr.tok[c];
+                ++j;
+                c = tr.ns[c];
+            }
+            if (j > 0 && s_len >= D) {   // a depth-D node has no children
+                if (writer) report(dev_status, DDT_DEV_BAD_TREE);
+                j = 0;
+            }
+            s_nkids = j;
+        }
+        __syncthreads();
+        const int nk = s_nkids;
+        const int len = s_len;
+        const float* drow = draft + (static_cast<size_t>(b) * D + (nk > 0 ? len : 0)) * static_cast<size_t>(V);
+        if (threadIdx.x < nk) {   // the children's logits and uniforms, one thread each
+            const int j = threadIdx.x;
+            const int x = s_kid_tok[j];
+            const bool ok = x >= 0 && x < V;
+            s_kid_l[j] = ok ? __ldg(row + x) : 0.0f;
+            s_kid_d[j] = ok ? __ldg(drow + x) : 0.0f;
+            const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(u),
+                                                     static_cast<uint32_t>(j), off_lo), k0, k1);
+            s_u[j] = uniform_exact(w.x);
+        }
+        // pass 1: (max, sum) of the target row and, with children, of the draft row
+        MaxSum mq{-INFINITY, 0.0f}, mp{-INFINITY, 0.0f};
+        if (vec4) {
+            const float4* r4 = reinterpret_cast<const float4*>(row);
+            const float4* d4 = reinterpret_cast<const float4*>(drow);
+#pragma unroll 2
+            for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads) {
+                const float4 f = __ldg(r4 + x);
+                ms_add(mq, f.x, inv_t); ms_add(mq, f.y, inv_t); ms_add(mq, f.z, inv_t); ms_add(mq, f.w, inv_t);
+                if (nk > 0) {
+                    const float4 g = __ldg(d4 + x);
+                    ms_add(mp, g.x, inv_t); ms_add(mp, g.y, inv_t); ms_add(mp, g.z, inv_t); ms_add(mp, g.w, inv_t);
+                }
+            }
+        } else {
+            for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads) {
+                ms_add(mq, __ldg(row + v), inv_t);
+                if (nk > 0) ms_add(mp, __ldg(drow + v), inv_t);
+            }
+        }
+        mq = block_ms(mq, inv_t, scratch_a, scratch_b);
+        mp = block_ms(mp, inv_t, scratch_a, scratch_b);
+        if (threadIdx.x == 0) part_s[round & 1] = make_float4(mq.m, mq.z, mp.m, mp.z);
+        cluster_barrier();
+        if (threadIdx.x == 0) {   // the same partials merged in the same order in every CTA
+            MaxSum aq{-INFINITY, 0.0f}, ap{-INFINITY, 0.0f};
+#pragma unroll
+            for (int r = 0; r < kCluster; ++r) {
+                const uint32_t a = cluster_addr(&part_s[round & 1], r);
+                const float2 q2 = ld_cluster_f32x2(a);
+                const float2 p2 = ld_cluster_f32x2(a + 8);
+                aq = merge_ms(aq, MaxSum{q2.x, q2.y}, inv_t);
+                ap = merge_ms(ap, MaxSum{p2.x, p2.y}, inv_t);
+            }
+            s_mq = aq.m; s_zq = aq.z; s_mp = ap.m; s_zp = ap.z;
+        }
+        ++round;
+        __syncthreads();
+        const float Mq = s_mq, rZq = 1.0f / s_zq, Mp = s_mp, rZp = nk > 0 ? 1.0f / s_zp : 0.0f;
+        // children in rank order against the residual max(q - c p, 0) / R
+        float c = 0.0f, R = 1.0f;
+        int match = -1;
+        for (int j = 0; j < nk; ++j) {
+            if (threadIdx.x == 0) {
+                int st;
+                const int x = s_kid_tok[j];
+                if (x < 0 || x >= V) {
+                    if (writer) report(dev_status, DDT_DEV_BAD_TOKEN);
+                    st = kSkip;
+                } else {
+                    const float qx = expf((s_kid_l[j] - Mq) * inv_t) * rZq;
+                    const float px = expf((s_kid_d[j] - Mp) * inv_t) * rZp;
+                    const float rx = fmaxf(qx - c * px, 0.0f) / R;
+                    st = s_u[j] * static_cast<double>(px) < static_cast<double>(rx) ? kAccept : kReject;
+                }
+                s_state = st;
+            }
+            __syncthreads();
+            const int st = s_state;
+            __syncthreads();   // every thread has read s_state before thread 0 writes it again
+            if (st == kAccept) { match = s_kid_node[j]; break; }
+            if (st == kSkip) continue;
+            c += R;
+            // the residual's mass for the next test, or to confirm the bonus has one
+            float part = 0.0f;
+            auto resid = [&](float l, float d) {
+                return fmaxf(expf((l - Mq) * inv_t) * rZq - c * (expf((d - Mp) * inv_t) * rZp), 0.0f);
+            };
+            if (vec4) {
+                const float4* r4 = reinterpret_cast<const float4*>(row);
+                const float4* d4 = reinterpret_cast<const float4*>(drow);
+#pragma unroll 2
+                for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads) {
+                    const float4 f = __ldg(r4 + x), g = __ldg(d4 + x);
+                    part += resid(f.x, g.x) + resid(f.y, g.y) + resid(f.z, g.z) + resid(f.w, g.w);
+                }
+            } else {
+                for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads)
+                    part += resid(__ldg(row + v), __ldg(drow + v));
+            }
+            part = block_sum_f(part, scratch_a);
+            if (threadIdx.x == 0) part_r[round & 1] = part;
+            cluster_barrier();
+            if (threadIdx.x == 0) {   // in rank order: the same sum in every CTA
+                float all = 0.0f;
+#pragma unroll
+                for (int r = 0; r < kCluster; ++r) all += ld_cluster_f32(cluster_addr(&part_r[round & 1], r));
+                s_R = all;
+            }
+            ++round;
+            __syncthreads();
+            R = s_R;
+            if (!(R > 0.0f)) {   // no residual mass left: the bonus comes from q
+                c = 0.0f;
+                break;
+            }
+        }
+        if (threadIdx.x == 0) {
+            const int l0 = s_len;
+            if (match != -1) {
+                if (writer) {
+                    toks[l0] = tr.tok[match];
+                    nodes[l0 + 1] = match;
+                }
+                s_len = l0 + 1;
+            }
+            s_next = match;
+        }
+        __syncthreads();
+        if (s_next != -1) { u = s_next; continue; }
+        // bonus: Gumbel-max of log max(q - c p, 0) over this CTA's slice; if no
+        // token keeps residual mass, once more with c = 0 (from q)
+        for (;;) {
+        unsigned long long best = 0ull;
+        const int g0 = vec4 ? sl.g0 : (sl.g0 >> 2), g1 = vec4 ? sl.g1 : ((sl.g1 + 3) >> 2);
+#pragma unroll 2
+        for (int x = g0 + static_cast<int>(threadIdx.x); x < g1; x += kWalkThreads) {
+            const uint4 w = philox4x32_10(make_uint4(1u | off_hi8, static_cast<uint32_t>(u),
+                                                     static_cast<uint32_t>(x), off_lo), k0, k1);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            float f[4], d[4];
+            if (vec4) {
+                const float4 t4 = __ldg(reinterpret_cast<const float4*>(row) + x);
+                f[0] = t4.x; f[1] = t4.y; f[2] = t4.z; f[3] = t4.w;
+                if (c > 0.0f) {
+                    const float4 d4 = __ldg(reinterpret_cast<const float4*>(drow) + x);
+                    d[0] = d4.x; d[1] = d4.y; d[2] = d4.z; d[3] = d4.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int v = 4 * x + e;
+                    f[e] = v < V ? __ldg(row + v) : 0.0f;
+                    d[e] = (v < V && c > 0.0f) ? __ldg(drow + v) : 0.0f;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int v = 4 * x + e;
+                if (v >= V || (!vec4 && (v < sl.g0 || v >= sl.g1))) continue;
+                float sc;
+                if (c > 0.0f) {
+                    const float r = expf((f[e] - Mq) * inv_t) * rZq - c * (expf((d[e] - Mp) * inv_t) * rZp);
+                    if (!(r > 0.0f)) continue;
+                    sc = logf(r);
+                } else {
+                    sc = (f[e] - Mq) * inv_t;   // log q up to a constant
+                }
+                sc += -logf(neg_log_uniform(ws[e]));
+                const unsigned long long p = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
+                best = best > p ? best : p;
+            }
+        }
+        best = block_reduce(best, scratch_u, MaxU64(), 0ull);
+        if (threadIdx.x == 0) part_g[round & 1] = best;
+        cluster_barrier();
+        if (threadIdx.x == 0) s_best = cluster_max_u64(&part_g[round & 1]);
+        ++round;
+        __syncthreads();
+        if (s_best == 0ull && c > 0.0f) {
+            c = 0.0f;
+            continue;
+        }
+        break;
+        }
+        if (threadIdx.x == 0 && writer) {
+            const unsigned long long all = s_best;
+            const int l0 = s_len;
+            const int32_t a = all ? static_cast<int32_t>(argmax_unpack_idx(all)) : -1;
+            toks[l0] = a;
+            o.bonus[b] = a;
+            o.accept_len[b] = l0;
+        }
+        break;
+    }
+    cluster_barrier();   // peers may still be reading this CTA's partials
+}
+
+cudaError_t launch_accept_ratio(const float* logits, const float* draft_logits, int V, const int32_t* token,
+                                const int32_t* first_child, const int32_t* next_sibling,
+                                const int32_t* n_nodes, int B, int N, int D, const float* temperature,
+                                const uint64_t* seed, uint64_t offset, int32_t* accept_len,
+                                int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
+                                int32_t* dev_status, cudaStream_t stream) {
+    const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
+                      (reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0);
+    WalkOut o{accept_len, out_tokens, out_nodes, bonus};
+    accept_ratio_kernel<<<B * kCluster, kWalkThreads, 0, stream>>>(
+        logits, draft_logits, V, vec4, token, first_child, next_sibling, n_nodes, N, D, temperature, seed,
+        offset, o, dev_status);
+    return cudaGetLastError();
+}
+
+}  // namespace ddt

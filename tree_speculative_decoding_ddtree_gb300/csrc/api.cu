@@ -19,6 +19,10 @@ cudaError_t launch_accept_sample(const float*, int, const int32_t*, const int32_
                                  const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*,
                                  int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_draft_topk(const float*, int, int, int, int, float*, int32_t*, cudaStream_t);
+cudaError_t launch_accept_ratio(const float*, const float*, int, const int32_t*, const int32_t*,
+                                const int32_t*, const int32_t*, int, int, int, const float*,
+                                const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*, int32_t*,
+                                int32_t*, cudaStream_t);
 cudaError_t launch_commit_kv(const ddtree_bf16*, const ddtree_bf16*, const int32_t*, const int32_t*, int,
                              int, int, int, int, ddtree_bf16*, ddtree_bf16*, int, int, const int32_t*,
                              int, const int32_t*, int32_t*, int32_t*, cudaStream_t);
@@ -226,6 +230,25 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                                          N, D, temperature, seed, philox_offset, accept_len,
                                          out_tokens, out_nodes, bonus, dev_status,
                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+int ddtree_accept_sample_ratio(const float* logits, const float* draft_logits, int V,
+                               const int32_t* token, const int32_t* first_child,
+                               const int32_t* next_sibling, const int32_t* n_nodes, int B, int N,
+                               int D, const float* temperature, const uint64_t* seed,
+                               uint64_t philox_offset, int32_t* accept_len, int32_t* out_tokens,
+                               int32_t* out_nodes, int32_t* bonus, int32_t* dev_status,
+                               void* stream) {
+    int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
+                             accept_len, out_tokens, out_nodes, bonus);
+    if (st != DDT_OK || B == 0) return st;
+    if (!draft_logits || !temperature || !seed) return DDT_EINVAL;
+    if (philox_offset >> 56) return DDT_EINVAL;
+    cudaError_t e = launch_accept_ratio(logits, draft_logits, V, token, first_child, next_sibling,
+                                        n_nodes, B, N, D, temperature, seed, philox_offset,
+                                        accept_len, out_tokens, out_nodes, bonus, dev_status,
+                                        static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
 

@@ -35,10 +35,15 @@ int record_step(const ddtree_step_args& a, cudaStream_t s) {
         st = ddtree_accept_greedy(a.logits, a.V, a.token, a.first_child, a.next_sibling, a.n_nodes,
                                   a.B, N, a.D, a.accept_len, a.out_tokens, a.out_nodes, a.bonus,
                                   a.dev_status, s);
-    else
+    else if (a.walk == 1)
         st = ddtree_accept_sample(a.logits, a.V, a.token, a.first_child, a.next_sibling, a.n_nodes,
                                   a.B, N, a.D, a.temperature, a.seed, a.philox_offset, a.accept_len,
                                   a.out_tokens, a.out_nodes, a.bonus, a.dev_status, s);
+    else
+        st = ddtree_accept_sample_ratio(a.logits, a.draft_logits, a.V, a.token, a.first_child,
+                                        a.next_sibling, a.n_nodes, a.B, N, a.D, a.temperature, a.seed,
+                                        a.philox_offset, a.accept_len, a.out_tokens, a.out_nodes,
+                                        a.bonus, a.dev_status, s);
     if (st != DDT_OK) return st;
     return ddtree_commit_kv(a.k_tree, a.v_tree, a.out_nodes, a.accept_len, a.B, N, a.D, a.Hkv, a.Dh,
                             a.k_cache, a.v_cache, a.num_pages, a.page_size, a.page_table,
@@ -55,7 +60,7 @@ size_t ddtree_step_args_size(void) { return sizeof(ddtree_step_args); }
 int ddtree_step_create(const ddtree_step_args* args, ddtree_step** out) {
     if (!out) return DDT_EINVAL;
     *out = nullptr;
-    if (!args || (args->walk != 0 && args->walk != 1)) return DDT_EINVAL;
+    if (!args || args->walk < 0 || args->walk > 2) return DDT_EINVAL;
     if (args->B < 1) return DDT_ESHAPE;   // an empty step has nothing to record
     cudaStream_t s = nullptr;
     cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);

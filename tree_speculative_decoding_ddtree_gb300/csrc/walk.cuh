@@ -1,0 +1,191 @@
+// Device helpers shared by the verify walks (greedy, sampled, draft-ratio):
+// thread-block cluster primitives, Philox4x32-10, block reductions, the
+// per-CTA vocabulary slices and the staged tree rows.
+#pragma once
+
+#include "common.cuh"
+
+namespace ddt {
+
+constexpr int kCluster = 8;               // CTAs per request (portable cluster size)
+constexpr int kWalkThreads = 512;
+constexpr int kMaxKids = DDT_MAX_TOPK;
+
+// ---------------------------------------------------------------------------
+// cluster helpers
+// ---------------------------------------------------------------------------
+DDT_DEVINL uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// every thread of every CTA of the cluster; orders shared-memory writes before
+// the barrier with reads after it, cluster-wide
+DDT_DEVINL void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// shared::cluster address of the same variable in CTA `rank`
+DDT_DEVINL uint32_t cluster_addr(const void* p, uint32_t rank) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+DDT_DEVINL unsigned long long ld_cluster_u64(uint32_t addr) {
+    unsigned long long v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];\n" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+DDT_DEVINL float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+DDT_DEVINL float2 ld_cluster_f32x2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon et al., SC'11): two multiply-xor lanes per round,
+// key bumped by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------
+DDT_DEVINL uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) { k0 += W0; k1 += W1; }
+        const uint32_t hi0 = __umulhi(M0, c.x), lo0 = M0 * c.x;
+        const uint32_t hi1 = __umulhi(M1, c.z), lo1 = M1 * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// -log(U) for U = ((w >> 8) + 0.5) * 2^-24, accurate in fp32 on both halves of
+// (0, 1): log of U below one half, log1p of -(1 - U) above it.
+DDT_DEVINL float neg_log_uniform(uint32_t w) {
+    const uint32_t k = w >> 8;
+    if (k < (1u << 23)) return -logf((static_cast<float>(k) + 0.5f) * 0x1p-24f);
+    const float one_minus_u = (static_cast<float>((1u << 24) - 1u - k) + 0.5f) * 0x1p-24f;
+    return -log1pf(-one_minus_u);
+}
+
+DDT_DEVINL double uniform_exact(uint32_t w) {
+    return (static_cast<double>(w >> 8) + 0.5) * 0x1p-24;
+}
+
+// block-wide reductions over kWalkThreads threads; every thread gets the result
+template <typename T, typename Op>
+DDT_DEVINL T block_reduce(T v, T* scratch, Op op, T identity) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        T x = lane < kWalkThreads / 32 ? scratch[lane] : identity;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x = op(x, __shfl_xor_sync(0xffffffffu, x, o));
+        if (lane == 0) scratch[0] = x;
+    }
+    __syncthreads();
+    return scratch[0];
+}
+
+struct MaxU64 { DDT_DEVINL unsigned long long operator()(unsigned long long a, unsigned long long b) const { return a > b ? a : b; } };
+
+// This CTA's slice of a row: float4 groups [g0, g1) when the row is read as
+// float4, else elements [g0, g1).
+struct Slice {
+    int g0, g1;
+};
+DDT_DEVINL Slice row_slice(int V, bool vec4, uint32_t rank) {
+    const int n = vec4 ? (V >> 2) : V;
+    Slice s;
+    s.g0 = static_cast<int>((static_cast<long long>(n) * rank) / kCluster);
+    s.g1 = static_cast<int>((static_cast<long long>(n) * (rank + 1)) / kCluster);
+    return s;
+}
+
+// argmax of this CTA's slice (largest value, lowest index, NaN lowest), packed
+DDT_DEVINL unsigned long long slice_argmax(const float* __restrict__ row, bool vec4, Slice sl,
+                                           unsigned long long* scratch) {
+    unsigned long long best = 0ull;
+    if (vec4) {
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 4
+        for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads) {
+            const float4 f = __ldg(r4 + x);
+            const uint32_t v = static_cast<uint32_t>(x) << 2;
+            unsigned long long p0 = argmax_pack(float_order_key(f.x), v);
+            unsigned long long p1 = argmax_pack(float_order_key(f.y), v + 1);
+            unsigned long long p2 = argmax_pack(float_order_key(f.z), v + 2);
+            unsigned long long p3 = argmax_pack(float_order_key(f.w), v + 3);
+            p0 = p0 > p1 ? p0 : p1;
+            p2 = p2 > p3 ? p2 : p3;
+            p0 = p0 > p2 ? p0 : p2;
+            best = best > p0 ? best : p0;
+        }
+    } else {
+        for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads) {
+            const unsigned long long p = argmax_pack(float_order_key(__ldg(row + v)), v);
+            best = best > p ? best : p;
+        }
+    }
+    return block_reduce(best, scratch, MaxU64(), 0ull);
+}
+
+// max over the cluster's partials (slot `part` in every CTA)
+DDT_DEVINL unsigned long long cluster_max_u64(const unsigned long long* part) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) {
+        const unsigned long long v = ld_cluster_u64(cluster_addr(part, r));
+        best = best > v ? best : v;
+    }
+    return best;
+}
+
+struct WalkOut {
+    int32_t* accept_len;
+    int32_t* out_tokens;
+    int32_t* out_nodes;
+    int32_t* bonus;
+};
+
+// The request's token / first-child / next-sibling rows, staged in shared
+// memory so the serial child scans never wait on global memory.
+struct TreeRows {
+    int tok[DDT_MAX_NODES];
+    int fc[DDT_MAX_NODES];
+    int ns[DDT_MAX_NODES];
+};
+
+DDT_DEVINL void stage_tree(TreeRows& t, const int32_t* token, const int32_t* first_child,
+                           const int32_t* next_sibling, size_t tb, int N) {
+    for (int i = threadIdx.x; i < N; i += kWalkThreads) {
+        t.tok[i] = token[tb + i];
+        t.fc[i] = first_child[tb + i];
+        t.ns[i] = next_sibling[tb + i];
+    }
+}
+
+// online (max, sum of exp((x - max) / T)) pair
+struct MaxSum {
+    float m, z;
+};
+
+DDT_DEVINL MaxSum merge_ms(MaxSum a, MaxSum b, float inv_t) {
+    const float M = fmaxf(a.m, b.m);
+    MaxSum r;
+    r.m = M;
+    r.z = (M == -INFINITY) ? 0.0f : a.z * expf((a.m - M) * inv_t) + b.z * expf((b.m - M) * inv_t);
+    return r;
+}
+
+}  // namespace ddt
