@@ -50,6 +50,7 @@ constexpr int kStages = 4;
 constexpr int kThreads = 512;
 constexpr int kD = 128;                   // head dim of this path
 constexpr int kMaxSide = 8;               // leftover rows handled on mma.sync
+constexpr int kLptMaxB = 64;              // batches up to this size run their longest chunks first
 
 constexpr uint32_t kQTileBytes = 128 * kD * 2;          // 32 KB (two 16 KB halves)
 constexpr uint32_t kHalfBytes = kKeys * 128;            // 8 KB: 64 rows x 128 B
@@ -86,6 +87,9 @@ struct TcShared {
     float side_max[2][4][kMaxSide];
     float side_l[4][kMaxSide];
     float side_m[kMaxSide];
+    int map_cnt[kLptMaxB];    // work-item counts in rank order (the CTA's item lookup)
+    int map_off[kLptMaxB];    // their exclusive prefix sums
+    int item[4];              // this CTA's (request, KV head, chunk, found)
 };
 
 struct Geometry {
@@ -120,6 +124,82 @@ DDT_DEVINL TileInfo tile_info(const Geometry& g, int j) {
 
 DDT_DEVINL uint32_t bar_addr(const uint64_t& b) { return smem_u32(&b); }
 
+// Context tiles of request b and its chunk count (1 for an empty or bad context).
+DDT_DEVINL void chunk_plan(const AttnParams& p, int b, int& nt, int& nch) {
+    const int L = p.ctx_len[b];
+    nt = (L < 0 || L > p.max_pages * p.page_size) ? 0 : (L + kKeys - 1) / kKeys;
+    nch = nt > 0 ? (nt + p.tiles_per_chunk - 1) / p.tiles_per_chunk : 1;
+}
+
+// Work item of CTA i when the batch runs longest chunks first (warp 0, all
+// lanes). Requests are ranked by their chunk length (tiles, descending; ties
+// by index); each contributes Hkv * nch items (head-major, then chunk), in
+// rank order. Writes (b, kvh, chunk, found) to `item`: found = 0 past the last
+// item. The CTAs are dispatched in index order, so the longest chunks start
+// first and the short ones fill the tail (longest processing time first).
+DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* item) {
+    const int lane = threadIdx.x & 31;
+    int key[2], nch[2], rnk[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int b = lane + 32 * q;
+        key[q] = -1;
+        nch[q] = 1;
+        if (b < p.B) {
+            int nt;
+            chunk_plan(p, b, nt, nch[q]);
+            key[q] = nt > 0 ? (nt + nch[q] - 1) / nch[q] : 0;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int b = lane + 32 * q;
+        int r = 0;
+        for (int s2 = 0; s2 < p.B; ++s2) {
+            const int ks = __shfl_sync(0xffffffffu, s2 < 32 ? key[0] : key[1], s2 & 31);
+            r += (ks > key[q]) || (ks == key[q] && s2 < b);
+        }
+        rnk[q] = r;
+        if (b < p.B) cnt[r] = nch[q] * p.Hkv;
+    }
+    __syncwarp();
+    // exclusive prefix over the ranked counts (two entries per lane)
+    const int c0 = 2 * lane < p.B ? cnt[2 * lane] : 0;
+    const int c1 = 2 * lane + 1 < p.B ? cnt[2 * lane + 1] : 0;
+    int incl = c0 + c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int excl = incl - c0 - c1;
+    off[2 * lane] = excl;
+    off[2 * lane + 1] = excl + c0;
+    __syncwarp();
+    int hit = -1, local = 0;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int b = lane + 32 * q;
+        if (b < p.B) {
+            const int o = off[rnk[q]];
+            if (i >= o && i < o + nch[q] * p.Hkv) { hit = q; local = i - o; }
+        }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
+    if (m) {
+        const int src = __ffs(m) - 1;
+        if (lane == src) {
+            const int b = lane + 32 * hit;
+            item[0] = b;
+            item[1] = local / nch[hit];
+            item[2] = local % nch[hit];
+            item[3] = 1;
+        }
+    } else if (lane == 0) {
+        item[3] = 0;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     extern __shared__ unsigned char smem_raw[];
@@ -130,9 +210,19 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     Geometry g;
-    g.b = blockIdx.z;
-    g.kvh = blockIdx.y;
-    g.chunk = blockIdx.x;
+    if (p.B <= kLptMaxB && p.max_chunks > 1) {   // one-dimensional grid, longest chunks first
+        if (warp == 0) lpt_item(p, static_cast<int>(blockIdx.x), sh.map_cnt, sh.map_off, sh.item);
+        __syncthreads();
+        if (!sh.item[3]) return;
+        g.b = sh.item[0];
+        g.kvh = sh.item[1];
+        g.chunk = sh.item[2];
+    } else {   // one-dimensional grid in (request, head, chunk) order
+        const int i = static_cast<int>(blockIdx.x);
+        g.chunk = i % p.max_chunks;
+        g.kvh = (i / p.max_chunks) % p.Hkv;
+        g.b = i / (p.max_chunks * p.Hkv);
+    }
     g.G = p.G;
     g.R = p.R;
     g.L = p.ctx_len[g.b];
@@ -143,8 +233,9 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     if (g.chunk >= g.nchunks) return;
     g.nn = p.n_nodes[g.b];
     if (g.nn < 0 || g.nn > p.N) { g.bad = true; g.nn = 0; }
-    g.t_begin = g.chunk * p.tiles_per_chunk;
-    g.n_ctx = max(0, min(nt_ctx, g.t_begin + p.tiles_per_chunk) - g.t_begin);
+    // the request's tiles in nchunks chunks of equal length (within one tile)
+    g.t_begin = static_cast<int>(static_cast<long long>(nt_ctx) * g.chunk / g.nchunks);
+    g.n_ctx = static_cast<int>(static_cast<long long>(nt_ctx) * (g.chunk + 1) / g.nchunks) - g.t_begin;
     g.n_tree = (g.chunk == g.nchunks - 1) ? (p.N + kKeys - 1) / kKeys : 0;
     g.n_tiles = g.n_ctx + g.n_tree;
     g.n_main = g.R > 128 ? 2 : 1;
@@ -777,8 +868,9 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    const dim3 grid(p.max_chunks, p.Hkv, p.B);
-    attn_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, maps);
+    const long long ctas = static_cast<long long>(p.max_chunks) * p.Hkv * p.B;
+    if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    attn_tc_kernel<<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
