@@ -89,7 +89,7 @@ struct TcShared {
     float side_m[kMaxSide];
     int map_cnt[kLptMaxB];    // work-item counts in rank order (the CTA's item lookup)
     int map_off[kLptMaxB];    // their exclusive prefix sums
-    int item[4];              // this CTA's (request, KV head, chunk, found)
+    int item[6];              // this CTA's (request, KV head, chunk, found, ctx_len, n_nodes)
 };
 
 struct Geometry {
@@ -139,15 +139,22 @@ DDT_DEVINL void chunk_plan(const AttnParams& p, int b, int& nt, int& nch) {
 // first and the short ones fill the tail (longest processing time first).
 DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* item) {
     const int lane = threadIdx.x & 31;
-    int key[2], nch[2], rnk[2];
+    int key[2], nch[2], rnk[2], Lq[2], nnq[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {   // the loads of both slots first, then the arithmetic
+        const int b = lane + 32 * q;
+        Lq[q] = b < p.B ? p.ctx_len[b] : 0;
+        nnq[q] = b < p.B ? p.n_nodes[b] : 0;
+    }
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
         const int b = lane + 32 * q;
         key[q] = -1;
         nch[q] = 1;
         if (b < p.B) {
-            int nt;
-            chunk_plan(p, b, nt, nch[q]);
+            const int L = Lq[q];
+            const int nt = (L < 0 || L > p.max_pages * p.page_size) ? 0 : (L + kKeys - 1) / kKeys;
+            nch[q] = nt > 0 ? (nt + p.tiles_per_chunk - 1) / p.tiles_per_chunk : 1;
             key[q] = nt > 0 ? (nt + nch[q] - 1) / nch[q] : 0;
         }
     }
@@ -194,6 +201,8 @@ DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* it
             item[1] = local / nch[hit];
             item[2] = local % nch[hit];
             item[3] = 1;
+            item[4] = Lq[hit];
+            item[5] = nnq[hit];
         }
     } else if (lane == 0) {
         item[3] = 0;
@@ -210,6 +219,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     Geometry g;
+    int nn_loaded;
     if (p.B <= kLptMaxB && p.max_chunks > 1) {   // one-dimensional grid, longest chunks first
         if (warp == 0) lpt_item(p, static_cast<int>(blockIdx.x), sh.map_cnt, sh.map_off, sh.item);
         __syncthreads();
@@ -217,21 +227,24 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         g.b = sh.item[0];
         g.kvh = sh.item[1];
         g.chunk = sh.item[2];
+        g.L = sh.item[4];
+        nn_loaded = sh.item[5];
     } else {   // one-dimensional grid in (request, head, chunk) order
         const int i = static_cast<int>(blockIdx.x);
         g.chunk = i % p.max_chunks;
         g.kvh = (i / p.max_chunks) % p.Hkv;
         g.b = i / (p.max_chunks * p.Hkv);
+        g.L = p.ctx_len[g.b];
+        nn_loaded = p.n_nodes[g.b];
     }
     g.G = p.G;
     g.R = p.R;
-    g.L = p.ctx_len[g.b];
     g.bad = false;
     if (g.L < 0 || g.L > p.max_pages * p.page_size) { g.bad = true; g.L = 0; }
     const int nt_ctx = (g.L + kKeys - 1) / kKeys;
     g.nchunks = nt_ctx > 0 ? (nt_ctx + p.tiles_per_chunk - 1) / p.tiles_per_chunk : 1;
     if (g.chunk >= g.nchunks) return;
-    g.nn = p.n_nodes[g.b];
+    g.nn = nn_loaded;
     if (g.nn < 0 || g.nn > p.N) { g.bad = true; g.nn = 0; }
     // the request's tiles in nchunks chunks of equal length (within one tile)
     g.t_begin = static_cast<int>(static_cast<long long>(nt_ctx) * g.chunk / g.nchunks);
@@ -569,9 +582,11 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             tc_fence_after();
             const int i = node, h = g.kvh * g.G + (valid_row ? r % g.G : 0);
             const bool good = done && ok;
+            // Rows leave through a per-warp staging block in the (now idle) Q region of
+            // shared memory, so that each store instruction writes whole rows.
+            uint32_t* stage = reinterpret_cast<uint32_t*>(smem + kOffQ) + (warp - 4) * (32 * 36);
             if (!split) {
                 const float inv = (real && good && l_sum > 0.0f) ? 1.0f / l_sum : 0.0f;
-                bf16_t* dst = p.out + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
@@ -584,31 +599,50 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                                                                  __uint_as_float(o[2 * e + 1]) * inv);
                         w[e] = *reinterpret_cast<uint32_t*>(&v);
                     }
-                    if (valid_row) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) =
-                                make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    for (int e = 0; e < 4; ++e)   // row stride 20 words: conflict-free 16-byte stores
+                        *reinterpret_cast<uint4*>(stage + lane * 20 + 4 * e) =
+                            make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {   // 8 rows x 64 bytes per instruction
+                        const int rr = 8 * k + (lane >> 2), q4 = lane & 3;
+                        const int rg = 128 * t + 32 * qw + rr;
+                        if (rg < g.R) {
+                            const int ir = rg / g.G, hr = g.kvh * g.G + rg % g.G;
+                            *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(g.b) * p.N + ir) * p.Hq + hr) * kD +
+                                                      32 * c + 8 * q4) =
+                                *reinterpret_cast<const uint4*>(stage + rr * 20 + 4 * q4);
+                        }
                     }
+                    __syncwarp();
                 }
                 if (p.lse && valid_row)
                     p.lse[(static_cast<size_t>(g.b) * p.N + i) * p.Hq + h] =
                         (real && good && l_sum > 0.0f) ? (m_ref + log2f(l_sum)) * 0.69314718055994531f
                                                        : -INFINITY;
             } else {
-                float* dst = p.ws_o + (slot * p.R + (valid_row ? r : 0)) * kD;
+                float* fst = reinterpret_cast<float*>(stage);
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
                     tmem_ld32(tO + 32 * c, o);
                     tmem_wait_ld();
-                    if (valid_row) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            *reinterpret_cast<float4*>(dst + 32 * c + 4 * e) =
-                                make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                            __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    for (int e = 0; e < 8; ++e)   // row stride 36 words: conflict-free 16-byte stores
+                        *reinterpret_cast<float4*>(fst + lane * 36 + 4 * e) =
+                            make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                        __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {   // 4 rows x 128 bytes per instruction
+                        const int rr = 4 * k + (lane >> 3), q4 = lane & 7;
+                        const int rg = 128 * t + 32 * qw + rr;
+                        if (rg < g.R)
+                            *reinterpret_cast<float4*>(p.ws_o + (slot * p.R + rg) * kD + 32 * c + 4 * q4) =
+                                *reinterpret_cast<const float4*>(fst + rr * 36 + 4 * q4);
                     }
+                    __syncwarp();
                 }
                 if (valid_row)
                     p.ws_ml[slot * p.R + r] = good ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.0f);
