@@ -43,7 +43,7 @@ METRIC = "tree-verify steps/s & attn HBM GB/s (% roofline), batch16 ctx8k budget
 # dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture (--set full,
 # one launch) of `bench.py --steps 5 --warmup 3 --no-cpu-baseline --e2e-steps 3`.
 # Taken on the current kernel; to be refreshed (or set to None) when it changes.
-ATTN_TC_TRAFFIC_BYTES = 533.478144e6 + 30.209280e6
+ATTN_TC_TRAFFIC_BYTES = 533.647360e6 + 25.676544e6
 WORKLOAD_DESC = ("batched serving: 16 requests, ctx ~U[1024,16384] paged (page 64, shuffled), "
                  "Hq 64 / Hkv 8 / Dh 128 bf16, budget 32 (N=33), top-k 8, depth 8, vocab 32000")
 
