@@ -124,13 +124,6 @@ DDT_DEVINL TileInfo tile_info(const Geometry& g, int j) {
 
 DDT_DEVINL uint32_t bar_addr(const uint64_t& b) { return smem_u32(&b); }
 
-// Context tiles of request b and its chunk count (1 for an empty or bad context).
-DDT_DEVINL void chunk_plan(const AttnParams& p, int b, int& nt, int& nch) {
-    const int L = p.ctx_len[b];
-    nt = (L < 0 || L > p.max_pages * p.page_size) ? 0 : (L + kKeys - 1) / kKeys;
-    nch = nt > 0 ? (nt + p.tiles_per_chunk - 1) / p.tiles_per_chunk : 1;
-}
-
 // Work item of CTA i when the batch runs longest chunks first (warp 0, all
 // lanes). Requests are ranked by their chunk length (tiles, descending; ties
 // by index); each contributes Hkv * nch items (head-major, then chunk), in

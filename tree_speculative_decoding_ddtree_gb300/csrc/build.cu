@@ -23,7 +23,6 @@ namespace ddt {
 
 constexpr int kMaxN = DDT_MAX_NODES;          // 128
 constexpr int kMaxW = (kMaxN + 31) / 32;      // 4
-constexpr int kSlots = kMaxN / 32;            // live heap entries <= 1 + budget <= 128
 
 struct BuildSmem {
     double n_score[kMaxN];
