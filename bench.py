@@ -248,6 +248,31 @@ def cpu_baseline_obj(res, n_slices):
 # reference arm
 # ---------------------------------------------------------------------------
 
+def rank_workload(name, rank, world):
+    """The batch rank `rank` runs: the named workload, its seed offset by the
+    rank when several ranks run (replicas: each GPU its own batch, no exchange)."""
+    import ddtree_synth as S
+    base = S.config(name)
+    return S.config(name, seed=base.seed + 7919 * rank) if world > 1 else base
+
+
+def max_over_ranks(x, world, device=None):
+    """The largest of the ranks' values of x (an elapsed time): all-reduce MAX
+    over the process group; x itself on one rank."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, seconds):
+    """Units per second of the whole job: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -297,8 +322,7 @@ def run_native(args):
     import ddtree_synth as S
     import tree_speculative_decoding_ddtree_gb300 as dd
 
-    base = S.config(args.config)
-    w = S.config(args.config, seed=base.seed + 7919 * rank) if world > 1 else base
+    w = rank_workload(args.config, rank, world)
 
     # CPU baseline first, in a fresh process (rank 0, N = 1 only)
     cpu_res = None
@@ -470,10 +494,7 @@ def run_native(args):
     e1.record(stream)
     torch.cuda.synchronize()
     per_call_us["ddtree_step_graph"] = e0.elapsed_time(e1) * 1e3 / 50
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     # end to end through the public API: host (pinned) inputs, copies in the timed
@@ -549,10 +570,7 @@ def run_native(args):
     t0 = time.perf_counter()
     e2e_run(args.e2e_steps)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        tt = torch.tensor([e2e_s], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks(e2e_s, world, device)
 
     if rank == 0:
         peaks = {}
@@ -564,7 +582,7 @@ def run_native(args):
         bf16_peak = peaks.get("bf16_tflops", 1900.0)
         peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
         ms_per_step = elapsed_ms / args.steps
-        value = world * args.steps / (elapsed_ms / 1e3)
+        value = whole_job_rate(world, args.steps, elapsed_ms / 1e3)
         abytes = algorithmic_attn_bytes(w, h["ctx"])
         aflops = algorithmic_attn_flops(w, h["ctx"], depth_sum)
         achieved = abytes / (attn_avg_ms * 1e-3) / 1e9
@@ -588,7 +606,7 @@ def run_native(args):
                          "algorithmic_bytes": abytes, "attn_us": attn_avg_ms * 1e3,
                          "tensor_tflops": aflops / (attn_avg_ms * 1e-3) / 1e12,
                          "tensor_frac_of_measured_bf16": aflops / (attn_avg_ms * 1e-3) / 1e12 / bf16_peak},
-            "e2e": {"value": world * args.e2e_steps / e2e_s, "unit": "steps/s",
+            "e2e": {"value": whole_job_rate(world, args.e2e_steps, e2e_s), "unit": "steps/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "note": ("KV cache stays resident (it is the cache); every step copies all of its inputs "
                              "in from pinned host memory and its results out; steps pipelined on two "
