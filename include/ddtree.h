@@ -112,8 +112,9 @@ const char* ddtree_last_error(void);
  *   topk_tok      int32 [B, D, K] their token ids
  * Ranking is by the logit (the same order as the log-prob), ties to the lower
  * token id, NaN below every number (-0 equals +0). The log-prob is the logit
- * minus the row's log-sum-exp, taken in fp64 from an fp32 exp-sum and rounded
- * to fp32 (about 1e-5 absolute from the fp64 value at V = 131072). A row
+ * minus the row's log-sum-exp (max + log of an fp32 exp-sum), formed in fp64
+ * and rounded to fp32; the error against the exact value is within
+ * (V/512 + 64) * 2^-22 + 2^-23 |log-prob| (about 1e-6 measured). A row
  * holding a NaN or +inf, or only -inf, has a NaN log-sum-exp: its K tokens
  * are still ranked and its log-probs are NaN.
  * 1 <= K <= min(32, V), 1 <= D <= 64, B * D < 2^31. Rows are read with 16-byte
