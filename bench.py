@@ -274,7 +274,7 @@ def whole_job_rate(world, units_per_rank, seconds):
 
 
 def run_reference(args):
-    rank, world, _ = dist_env()
+    rank, _, _ = dist_env()
     if rank != 0:
         return
     import ddtree_synth as S
