@@ -7,15 +7,18 @@
 // Constraint (load contexts once).
 //
 // One CTA owns every query row of one (request, KV head) and one chunk of its
-// context. Its R = N * G rows (node-major: row r = node r / G, head r % G)
-// are two 128-row tensor-core tiles plus up to 8 leftover rows:
+// context (a request's context is cut into chunks of equal length; with a
+// split context, warp 0 of each CTA first maps the block index to a work
+// item so that the longest chunks are dispatched first). Its R = N * G rows
+// (node-major: row r = node r / G, head r % G) are two 128-row tensor-core
+// tiles plus up to 8 leftover rows:
 //
 //   warp 0       TMA producer: Q once, then paged K/V tiles of 64 keys (one
 //                page box per half of the head dim, 128-byte swizzle) into a
 //                4-stage ring; zeroes V rows past the valid keys of a ragged
 //                tile so masked keys contribute exact zeros.
 //   warp 1       allocates TMEM; one lane issues tcgen05.mma:
-//                S_t = Q_t K^T (both K-major in shared memory) and
+//                S_t = Q_t K^T (Q from TMEM, K K-major in shared memory) and
 //                O_t += P_t V (P from TMEM, V MN-major in shared memory),
 //                ping-ponging the two tiles so the tensor core works on one
 //                tile while the other tile's softmax runs.
@@ -23,7 +26,9 @@
 //   warps 8-11   S, mask (context tail, ancestor bitmask on the tree tile),
 //                online softmax in the exp2 domain with a lazy rescale of O
 //                (only when the running max grows by more than 2^8), write P
-//                as bf16 over S in TMEM; final normalisation and store.
+//                as bf16 over S in TMEM; final normalisation and store, staged
+//                per warp through the (then idle) Q region of shared memory
+//                so that every store instruction writes whole rows.
 //   warps 12-15  the leftover rows on mma.sync (keys on M, rows on N), reading
 //                the same K/V stages through ldmatrix.
 //
