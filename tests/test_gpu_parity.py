@@ -73,6 +73,8 @@ def _random_topk(seed, B, D, K, V=5000, ties=False):
     (5, 4, 3, 0, False),       # budget 0: root only
     (4, 64, 32, 127, False),   # largest tree, widest cap, deepest draft
     (6, 6, 4, 50, True),       # many equal scores: push order decides
+    (3, 5, 3, 20, True),       # equal scores, one-slot heap
+    (4, 16, 8, 100, True),     # equal scores, four-slot heap
     (33, 5, 5, 31, True),      # more requests than one block holds
     (1, 2, 2, 10, False),      # every candidate fits
 ])

@@ -15,8 +15,9 @@
 // That is the heap's total order (score descending, earlier push first), so a
 // pop takes entry 0 and an insert lands after every entry with a key >= its
 // own: one ballot and one shift. Only lane 0 touches fp64 (two adds per pop,
-// in path order, as in the definition). Masks, positions and child links are
-// then computed with every lane working on its own nodes.
+// in path order, as in the definition); it also records each node's first
+// child and next sibling as nodes are added. Masks and positions are then
+// computed with every lane working on its own nodes.
 #include "common.cuh"
 
 namespace ddt {
@@ -30,6 +31,8 @@ struct BuildSmem {
     int n_depth[kMaxN];
     int n_rank[kMaxN];
     int n_token[kMaxN];
+    int n_first_child[kMaxN];
+    int n_next_sibling[kMaxN];
 };
 
 // order-preserving key of a double (NaN ranks as -inf); 0 is below every key.
@@ -44,10 +47,17 @@ DDT_DEVINL double key_score(unsigned long long k) {
     return __longlong_as_double(static_cast<long long>(b));
 }
 
+// entry code: depth << 24 | previous sibling << 16 | rank << 8 | parent
+// (depth <= 64, node indices <= 127, rank <= 31: each fits its byte)
+DDT_DEVINL uint32_t entry_code(int d, int prev, int r, int p) {
+    return (static_cast<uint32_t>(d) << 24) | (static_cast<uint32_t>(prev) << 16) |
+           (static_cast<uint32_t>(r) << 8) | static_cast<uint32_t>(p);
+}
+
 template <int SLOTS>
 struct WarpHeap {
     unsigned long long key[SLOTS];
-    uint32_t code[SLOTS];   // depth << 16 | rank << 8 | parent
+    uint32_t code[SLOTS];   // entry_code()
 
     DDT_DEVINL void clear() {
 #pragma unroll
@@ -91,7 +101,10 @@ struct WarpHeap {
 };
 
 // lp: the request's top-k log-probs, already widened to fp64 (exactly), so
-// the loop's only fp64 instructions are the two independent score adds per pop
+// the loop's only fp64 instructions are the two independent score adds per pop.
+// A node's first child is its rank-0 child and the next sibling of a rank-r
+// node the rank-(r+1) node it pushed (a sibling is pushed only when the one
+// before it is added), so both links are known when a node is added.
 template <int SLOTS>
 DDT_DEVINL int build_pops(BuildSmem& s, const double* lp, const int32_t* tk, int D, int K, int budget,
                           int lane) {
@@ -99,7 +112,7 @@ DDT_DEVINL int build_pops(BuildSmem& s, const double* lp, const int32_t* tk, int
     h.clear();
     int count = 0, live = 0;
     if (budget >= 1) {
-        h.insert(score_key(0.0 + lp[0]), (1u << 16) | (0u << 8) | 0u, lane);
+        h.insert(score_key(0.0 + lp[0]), entry_code(1, 0, 0, 0), lane);
         live = 1;
     }
     while (count < budget && live > 0) {
@@ -107,8 +120,8 @@ DDT_DEVINL int build_pops(BuildSmem& s, const double* lp, const int32_t* tk, int
         const uint32_t code = __shfl_sync(0xffffffffu, h.code[0], 0);
         h.pop_front(lane);
         --live;
-        const int d = static_cast<int>(code >> 16), r = static_cast<int>((code >> 8) & 0xffu),
-                  p = static_cast<int>(code & 0xffu);
+        const int d = static_cast<int>(code >> 24), q = static_cast<int>((code >> 16) & 0xffu),
+                  r = static_cast<int>((code >> 8) & 0xffu), p = static_cast<int>(code & 0xffu);
         ++count;
         const int i = count;
         double cs = 0.0, ss = 0.0;
@@ -119,18 +132,19 @@ DDT_DEVINL int build_pops(BuildSmem& s, const double* lp, const int32_t* tk, int
             s.n_depth[i] = d;
             s.n_rank[i] = r;
             s.n_token[i] = tk[(d - 1) * K + r];
+            if (r == 0) s.n_first_child[p] = i;
+            else s.n_next_sibling[q] = i;
             if (d < D) cs = sc + lp[d * K];                                 // best child
             if (r + 1 < K) ss = s.n_score[p] + lp[(d - 1) * K + r + 1];      // next sibling
         }
         const unsigned long long ck = __shfl_sync(0xffffffffu, score_key(cs), 0);
         const unsigned long long sk = __shfl_sync(0xffffffffu, score_key(ss), 0);
         if (d < D) {   // the child is pushed before the sibling
-            h.insert(ck, (static_cast<uint32_t>(d + 1) << 16) | (0u << 8) | static_cast<uint32_t>(i), lane);
+            h.insert(ck, entry_code(d + 1, 0, 0, i), lane);
             ++live;
         }
         if (r + 1 < K) {
-            h.insert(sk, (static_cast<uint32_t>(d) << 16) | (static_cast<uint32_t>(r + 1) << 8) |
-                             static_cast<uint32_t>(p), lane);
+            h.insert(sk, entry_code(d, i, r + 1, p), lane);
             ++live;
         }
         __syncwarp();
@@ -169,6 +183,7 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
         s.n_rank[0] = 0;
         s.n_token[0] = root_tok[b];
     }
+    for (int i = lane; i < N; i += 32) { s.n_first_child[i] = -1; s.n_next_sibling[i] = -1; }
     __syncwarp();
 
     int count;
@@ -182,27 +197,17 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
     const size_t base = static_cast<size_t>(b) * N;
     for (int i = lane; i < N; i += 32) {
         const bool real = i < n;
-        int fc = -1, ns = -1;
         uint32_t vw[kMaxW] = {0u, 0u, 0u, 0u};
-        if (real) {
-            // children in index order = rank order: first child, next sibling
-            for (int c = i + 1; c < n; ++c)
-                if (s.n_parent[c] == i) { fc = c; break; }
-            const int pi = s.n_parent[i];
-            if (pi >= 0)
-                for (int c = i + 1; c < n; ++c)
-                    if (s.n_parent[c] == pi) { ns = c; break; }
-            // ancestor-or-self bits
+        if (real)   // ancestor-or-self bits
             for (int a = i; a >= 0; a = s.n_parent[a]) vw[a >> 5] |= 1u << (a & 31);
-        }
         parent[base + i] = real ? s.n_parent[i] : -1;
         depth[base + i] = real ? s.n_depth[i] : -1;
         token[base + i] = real ? s.n_token[i] : -1;
         rank[base + i] = real ? s.n_rank[i] : -1;
         pos[base + i] = real ? L + s.n_depth[i] : -1;
         score[base + i] = real ? s.n_score[i] : -INFINITY;
-        first_child[base + i] = fc;
-        next_sibling[base + i] = ns;
+        first_child[base + i] = real ? s.n_first_child[i] : -1;
+        next_sibling[base + i] = real ? s.n_next_sibling[i] : -1;
         for (int w = 0; w < W; ++w) vis[(base + i) * W + w] = vw[w];
     }
     if (lane == 0) n_nodes_out[b] = n;
