@@ -222,6 +222,34 @@ def test_attn_full_size_sampled(name, picks):
         check_attn(got[b, :, kvh * G:(kvh + 1) * G, :], oracle_slice(st, b, kvh), f"{name} b={b} kv={kvh}")
 
 
+def test_attn_rescale_for_some_rows_of_a_warp():
+    """A context key equal to 1.5 x one row's query lifts that row's running max
+    by far more than 2^8 in the middle of a chunk, while the other rows of its
+    warp keep theirs: the online softmax rescales O for some rows of a warp only."""
+    st = stage(S.config("batched"), logits=False)
+    w = st.w
+    G, ps = w.G, w.page_size
+    b, kvh = 3, 2
+    L = int(st.ctx[b])
+    kc, vc = st.kv["k_cache"], st.kv["v_cache"]
+    targets = [(2, 1), (9, 6), (20, 0), (30, 5), (32, 2)]   # (node, head in group): both tiles + leftover
+    v_mark = S.f32_to_bf16_bits(np.full(w.Dh, 3.0, np.float32))
+    for k, (u, g) in enumerate(targets):
+        i = L * (k + 1) // 6 + 11
+        page, slot = int(st.table[b, i // ps]), i % ps
+        kc[page, slot, kvh, :] = S.f32_to_bf16_bits(1.5 * S.bf16_bits_to_f32(st.qkv["q"][b, u, kvh * G + g, :]))
+        vc[page, slot, kvh, :] = v_mark
+    s = status()
+    out, _ = run_attn(st, stat=s)
+    assert int(s.item()) == 0
+    got = out.float().cpu().numpy().astype(np.float64)[b, :, kvh * G:(kvh + 1) * G, :]
+    ref = oracle_slice(st, b, kvh)
+    for u, g in targets:
+        if u < int(st.tree.n_nodes[b]):
+            assert ref[u, g].mean() > 2.0          # the planted key dominates that row
+    check_attn(got, ref, "planted keys")
+
+
 @pytest.mark.slow
 def test_attn_deep_sampled():
     st = stage(S.config("deep"), logits=False)

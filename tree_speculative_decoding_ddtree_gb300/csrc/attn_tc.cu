@@ -541,10 +541,16 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                            fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             }
             const float mxs = mx * sc;
-            if (mxs > m_ref + 8.0f) {   // raise the reference: rescale O and l
-                if (j > 0 && m_ref != -INFINITY) {
+            // Raise the reference max of a row when it grows by more than 2^8, and
+            // rescale O and l. The decision is taken for the whole warp (the
+            // TMEM loads and stores are warp-collective): rows that need no
+            // rescale keep their reference and scale by exactly 1.
+            const bool raise = mxs > m_ref + 8.0f;
+            if (__any_sync(0xffffffffu, raise)) {
+                const float m_new = raise ? mxs : m_ref;
+                if (j > 0) {
                     // QK_t(j) was issued after PV_t(j-1), so S ready means O is complete
-                    const float alpha = fast_exp2(m_ref - mxs);
+                    const float alpha = (raise && m_ref != -INFINITY) ? fast_exp2(m_ref - m_new) : 1.0f;
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
@@ -556,7 +562,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                     }
                     l_sum *= alpha;
                 }
-                m_ref = mxs;
+                m_ref = m_new;
             }
             const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
             // P = 2^(s*scale - m) as bf16 pairs over the first 32 columns of this S buffer
