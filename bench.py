@@ -251,6 +251,13 @@ def cpu_baseline_obj(res, n_slices):
 # reference arm
 # ---------------------------------------------------------------------------
 
+def mean_context(w):
+    """The workload's mean context length in tokens (its seeded lengths), the
+    `seq_len` both arms report."""
+    import ddtree_synth as S
+    return int(S.context_lengths(w).sum()) // w.B
+
+
 def rank_workload(name, rank, world):
     """The batch rank `rank` runs: the named workload, its seed offset by the
     rank when several ranks run (replicas: each GPU its own batch, no exchange)."""
@@ -294,7 +301,7 @@ def run_reference(args):
             "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, ddtree_synth)",
             "config": {"workload": WORKLOAD_DESC if args.config == "batched" else args.config,
-                       "global_batch": w.B, "seq_len": "ctx U[1024,16384] + 33 tree rows",
+                       "global_batch": w.B, "seq_len": mean_context(w),
                        "parallelism": "single process"},
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
                              "sample": ("each step: the fp64 oracle's full build and both accept "
@@ -596,7 +603,7 @@ def run_native(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded, ddtree_synth)",
             "config": {"workload": WORKLOAD_DESC if w.name == "batched" else w.name,
-                       "global_batch": w.B * world, "seq_len": int(h["ctx"].sum()) // w.B,
+                       "global_batch": w.B * world, "seq_len": mean_context(w),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (paged KV cache %.0f MB > 129 MB L2)"
                              % (h["kv"]["k_cache"].nbytes * 2 / 1e6)},

@@ -77,3 +77,21 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_0():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_line_carries_the_contract_keys():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--config", "tiny"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    sys.path.insert(0, ROOT)
+    import bench
+    import ddtree_synth as S
+    w = S.config("tiny")
+    assert line["config"]["workload"] == "tiny" and line["config"]["global_batch"] == w.B
+    assert line["config"]["seq_len"] == bench.mean_context(w) == 256   # the tiny workload's fixed context
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["value"] == line["value"]
