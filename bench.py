@@ -251,6 +251,74 @@ def cpu_baseline_obj(res, n_slices):
 # reference arm
 # ---------------------------------------------------------------------------
 
+# Each reference step is a sample sized from a time budget for the whole run:
+# build + greedy + sampled walk for n_req of the B requests (cycled), and the
+# oracle attention of one random (request, KV head) slice over the first n_keys
+# of its context keys plus its tree rows. Both are scaled to the whole step,
+# linearly in requests and in attended keys (context + tree rows, all slices).
+REF_SNIPPET = r"""
+import dataclasses, json, math, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import ddtree_synth as S
+import oracle as O
+w = S.config({name!r})
+reps, budget_s = {reps}, {budget_s}
+dl, root, _ = S.draft_inputs(w)
+ctx = S.context_lengths(w)
+table, npg = S.paged_layout(w, ctx)
+qkv = S.qkv_tree(w)
+kv = S.kv_cache(w, npg)
+lp, tok = O.draft_topk(dl, w.K)
+tree0 = O.build_tree(lp, tok, root, ctx, w.budget)
+logits = S.target_logits(w, dl, tree0.depth, tree0.n_nodes)
+temp, seed = S.sampling_params(dataclasses.replace(w, temperature=0.7))
+f = O.bf16_to_f64
+G = w.G
+vis0 = O.unpack_vis(tree0.vis, w.N)
+all_keys = (int(ctx.sum()) + w.B * w.N) * w.Hkv
+
+def one_request(b):
+    t0 = time.perf_counter()
+    tr = O.build_tree(lp[b:b+1], tok[b:b+1], root[b:b+1], ctx[b:b+1], w.budget)
+    O.accept_greedy(logits[b:b+1], tr, w.D)
+    O.accept_sample(logits[b:b+1], tr, w.D, temp[b:b+1], seed[b:b+1], 0)
+    return time.perf_counter() - t0
+
+def one_slice(b, kvh, n_keys):
+    L = min(int(ctx[b]), n_keys)
+    npb = -(-L // w.page_size)
+    pages = table[b, :max(npb, 1)]
+    t0 = time.perf_counter()
+    kc = f(kv["k_cache"][pages][:, :, kvh:kvh + 1, :]); vc = f(kv["v_cache"][pages][:, :, kvh:kvh + 1, :])
+    O.tree_verify_attention(f(qkv["q"][b:b+1, :, kvh*G:(kvh+1)*G]), f(qkv["k_tree"][b:b+1, :, kvh:kvh+1]),
+                            f(qkv["v_tree"][b:b+1, :, kvh:kvh+1]), kc, vc,
+                            np.arange(max(npb, 1), dtype=np.int32)[None], np.array([L], np.int32),
+                            vis0[b:b+1], tree0.n_nodes[b:b+1], 1 / math.sqrt(w.Dh), w.page_size)
+    return time.perf_counter() - t0, L + w.N
+
+# calibration, untimed: one request, one slice of up to 256 context keys
+t_req = one_request(0)
+t_a, k_a = one_slice(int(np.argmax(ctx)), 0, 256)
+per_step = budget_s / reps
+n_req = max(1, min(w.B, int(0.4 * per_step / max(t_req, 1e-6))))
+n_keys = max(64, min(int(ctx.max()), int(0.4 * per_step * k_a / max(t_a, 1e-6))))
+rng = np.random.default_rng(0)
+out, nb = [], 0
+for rep in range(reps):
+    t_r = 0.0
+    for _ in range(n_req):
+        t_r += one_request(nb % w.B)
+        nb += 1
+    b, kvh = int(rng.integers(w.B)), int(rng.integers(w.Hkv))
+    t_s, keys = one_slice(b, kvh, n_keys)
+    out.append(dict(step_s=t_r * w.B / n_req + t_s * all_keys / keys, n_req=n_req, n_keys=n_keys))
+print(json.dumps(out))
+"""
+
+# seconds of oracle work the reference arm may spend on its K + W steps
+REF_BUDGET_S = 120.0
+
 def mean_context(w):
     """The workload's mean context length in tokens (its seeded lengths), the
     `seq_len` both arms report."""
@@ -289,10 +357,19 @@ def run_reference(args):
         return
     import ddtree_synth as S
     w = S.config(args.config)
-    n_sl = 2
+    n_reps = max(args.warmup, 0) + args.steps
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = REF_SNIPPET.format(root=ROOT, name=args.config, reps=n_reps, budget_s=REF_BUDGET_S)
     t0 = time.perf_counter()
-    reps = run_cpu_oracle(args.config, n_sl, reps=max(args.warmup, 0) + args.steps)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=3 * REF_BUDGET_S + 900)
     elapsed = time.perf_counter() - t0
+    if r.returncode != 0:
+        raise RuntimeError("oracle reference arm failed: " + r.stderr[-2000:])
+    reps = json.loads(r.stdout.strip().splitlines()[-1])
     per = [r["step_s"] for r in reps[max(args.warmup, 0):]]
     step_s = sum(per) / len(per)
     value = 1.0 / step_s
@@ -304,10 +381,14 @@ def run_reference(args):
                        "global_batch": w.B, "seq_len": mean_context(w),
                        "parallelism": "single process"},
             "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                             "sample": ("each step: the fp64 oracle's full build and both accept "
-                                        f"walks for all {w.B} requests, attention on {n_sl} random "
-                                        "(request, KV head) slices scaled to the batch by key "
-                                        "count; 1 thread")},
+                             "sample": (f"each step: the fp64 oracle's build, greedy and sampled walk for "
+                                        f"{reps[0]['n_req']} of {w.B} requests (cycled) and its attention "
+                                        f"on one random (request, KV head) slice over up to "
+                                        f"{reps[0]['n_keys']} context keys plus the tree rows, scaled to "
+                                        "the whole step linearly in requests and attended keys; the "
+                                        f"sample is sized for at most about {REF_BUDGET_S:.0f} s over the "
+                                        f"{n_reps} steps (capped at the whole batch and the longest "
+                                        "context); 1 thread")},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s": elapsed}
