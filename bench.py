@@ -33,6 +33,7 @@ import math
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -61,6 +62,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-slices", type=int, default=4)
+    ap.add_argument("--clocks-dir", default="",
+                    help="folder for the raw nvidia-smi clock samples (default: the system temp folder)")
     return ap.parse_args()
 
 
@@ -116,10 +119,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, out_dir: str = ""):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(out_dir or tempfile.gettempdir(), f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
         try:
@@ -539,7 +542,7 @@ def run_native(args):
     torch.cuda.synchronize()
     barrier()
     launches_per_step = 4 + (1 if ws_bytes > 0 else 0)
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, args.clocks_dir) as clk:
         torch.cuda.synchronize()
         barrier()
         t_start = torch.cuda.Event(enable_timing=True)
