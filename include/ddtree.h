@@ -218,7 +218,9 @@ int tree_verify_attn(const ddtree_bf16* q, const ddtree_bf16* k_tree,
 
 /* Bytes of workspace tree_verify_attn needs for these sizes when every
  * context is at most max_ctx tokens (max_ctx = max_pages * page_size covers
- * any page table). Returns 0 for unsupported sizes. */
+ * any page table). Returns 0 for unsupported sizes. The split-KV plan is
+ * sized in waves of the current device's SM count (queried once per
+ * device), so ask with the device current that will run the call. */
 size_t tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int Dh,
                                        int max_ctx);
 
@@ -443,7 +445,10 @@ void ddtree_step_destroy(ddtree_step* step);
  * - Sizes whose scratch need (tree_verify_attn_workspace_size) exceeds the
  *   array are rejected with DDT_ESCRATCH before anything is launched.
  * - The first call on each device looks up the array's device address with
- *   that device current; make that first call before any stream capture.
+ *   that device current and caches it with the id of the current CUDA
+ *   context; a call under another context (after cudaDeviceReset, say)
+ *   looks it up again. Make the first call on a device, and the first after
+ *   a reset, before any stream capture.
  * - All calls share the array and it keeps the last call's contents; every
  *   scratch word a call reads is written earlier in the same call, so nothing
  *   is cleared. Calls that overlap on the GPU (unordered streams, or several

@@ -68,10 +68,11 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     # Hq/Hkv = 6 does not divide 128, so the warp-MMA kernel takes the call:
     # 96 nodes x 6 heads = 576 rows (two row groups of 288) over up to 256k
     # tokens of context need more split-KV scratch than the array holds. The
-    # need is checked with the library's own workspace_size first, and the
-    # entry point is called (with placeholder pointers) only when it exceeds
-    # the array: the call must then return DDT_ESCRATCH on the host, before
-    # anything is launched.
+    # need is checked with the library's own workspace_size first. Every
+    # pointer is NULL: the entry point must return DDT_ESCRATCH on the host
+    # before anything is launched, and if that check were ever lost the
+    # attention call behind it would refuse the NULL pointers with DDT_EINVAL,
+    # again on the host, so no kernel can be handed a bad address.
     lib = dd.load_library()
     B, N, Hq, Hkv, Dh, page, max_pages = 2, 96, 48, 8, 128, 64, 4096
     cap = lib.tree_verify_attn_noalloc_max_scratch
@@ -82,8 +83,8 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     fn.restype = I
     fn.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P, I, I, I, I, I, F, P, P, P, P]
-    fake = 4096
-    st = fn(fake, fake, fake, fake, fake, 16 * max_pages, page, fake, max_pages, fake, fake, fake,
-            B, N, Hq, Hkv, Dh, 0.1, fake, 0, 0, 0)
+    null = None
+    st = fn(null, null, null, null, null, 16 * max_pages, page, null, max_pages, null, null, null,
+            B, N, Hq, Hkv, Dh, 0.1, null, null, null, null)
     assert st == -7
     assert b"scratch" in lib.ddtree_status_string(-7)

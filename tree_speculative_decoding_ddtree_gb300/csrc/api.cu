@@ -1,11 +1,13 @@
 // C ABI of the DDTree verify step: host-side argument checks, then launches.
 // Nothing here allocates or synchronises; every call is stream-ordered.
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
 
 #include "attn.cuh"
 #include "common.cuh"
+#include "trace.h"
 
 namespace ddt {
 cudaError_t launch_build(const float*, const int32_t*, const int32_t*, const int32_t*, int, int,
@@ -40,8 +42,29 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-constexpr int kPlanSMs = 152;        // GB300 SM count used to size the split-KV grid
 constexpr int kPlanWaves = 3;        // target CTAs per SM over a full-length batch (3 measured best of 2..8)
+constexpr int kMaxPlanDevices = 64;
+constexpr int kHostOnlySMs = 152;    // sizing on a host without a usable device (nothing launches there)
+
+// SM count of the current device, queried once per device: the split-KV grid
+// is sized in waves of it.
+int plan_sms() {
+    static std::atomic<int> cache[kMaxPlanDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxPlanDevices) {
+        cudaGetLastError();
+        return kHostOnlySMs;
+    }
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+            cudaGetLastError();
+            return kHostOnlySMs;
+        }
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
 constexpr int kKeyTile = 64;
 
 struct AttnPlan {
@@ -63,13 +86,14 @@ bool plan_attn(int B, int N, int Hq, int Hkv, int Dh, long long max_ctx, AttnPla
     if (pl->rows_per_group > kMaxRowsPerCta) pl->rows_per_group = kMaxRowsPerCta;
     const long long tiles = (max_ctx + kKeyTile - 1) / kKeyTile;
     const long long total = static_cast<long long>(B) * Hkv * pl->n_groups * (tiles > 0 ? tiles : 1);
-    long long tpc = (total + kPlanSMs * kPlanWaves - 1) / (kPlanSMs * kPlanWaves);
+    const long long slots = static_cast<long long>(plan_sms()) * kPlanWaves;
+    long long tpc = (total + slots - 1) / slots;
     if (tpc < 4) tpc = 4;
     pl->tiles_per_chunk = static_cast<int>(tpc);
     pl->max_chunks = tiles > 0 ? static_cast<int>((tiles + tpc - 1) / tpc) : 1;
-    const size_t slots = static_cast<size_t>(B) * Hkv * pl->max_chunks * R;
-    pl->ws_o_bytes = pl->max_chunks > 1 ? (slots * Dh * sizeof(float) + 255) / 256 * 256 : 0;
-    pl->ws_ml_bytes = pl->max_chunks > 1 ? (slots * sizeof(float2) + 255) / 256 * 256 : 0;
+    const size_t rows = static_cast<size_t>(B) * Hkv * pl->max_chunks * R;
+    pl->ws_o_bytes = pl->max_chunks > 1 ? (rows * Dh * sizeof(float) + 255) / 256 * 256 : 0;
+    pl->ws_ml_bytes = pl->max_chunks > 1 ? (rows * sizeof(float2) + 255) / 256 * 256 : 0;
     return true;
 }
 
@@ -104,6 +128,7 @@ const char* ddtree_last_error(void) { return g_last_error; }
 
 int ddtree_draft_topk(const float* draft_logits, int B, int D, int V, int K, float* topk_logp,
                       int32_t* topk_tok, void* stream) {
+    TraceRange trace("ddtree_draft_topk");
     if (B < 0 || V < 1) return DDT_EINVAL;
     if (K < 1 || K > DDT_MAX_TOPK || K > V || D < 1 || D > DDT_MAX_DEPTH ||
         static_cast<long long>(B) * D > 0x7FFFFFFFll)
@@ -120,6 +145,7 @@ int ddtree_build(const float* topk_logp, const int32_t* topk_tok, const int32_t*
                  int32_t* depth, int32_t* token, int32_t* rank, int32_t* pos, double* score,
                  int32_t* first_child, int32_t* next_sibling, uint32_t* vis, int32_t* n_nodes,
                  int32_t* dev_status, void* stream) {
+    TraceRange trace("ddtree_build");
     if (B < 0) return DDT_EINVAL;
     if (K < 1 || K > DDT_MAX_TOPK || D < 1 || D > DDT_MAX_DEPTH || budget < 0 ||
         budget + 1 > DDT_MAX_NODES)
@@ -147,6 +173,7 @@ int tree_verify_attn(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtr
                      int B, int N, int Hq, int Hkv, int Dh, float scale, ddtree_bf16* out,
                      float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                      void* stream) {
+    TraceRange trace("tree_verify_attn");
     if (B < 0 || !std::isfinite(scale)) return DDT_EINVAL;
     if (page_size < 16 || page_size > 1024 || page_size % 16 != 0 || num_pages < 1 ||
         max_pages < 1)
@@ -206,6 +233,7 @@ int ddtree_accept_greedy(const float* logits, int V, const int32_t* token,
                          const int32_t* n_nodes, int B, int N, int D, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
                          int32_t* dev_status, void* stream) {
+    TraceRange trace("ddtree_accept_greedy");
     int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
                              accept_len, out_tokens, out_nodes, bonus);
     if (st != DDT_OK || B == 0) return st;
@@ -221,6 +249,7 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                          const uint64_t* seed, uint64_t philox_offset, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
                          int32_t* dev_status, void* stream) {
+    TraceRange trace("ddtree_accept_sample");
     int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
                              accept_len, out_tokens, out_nodes, bonus);
     if (st != DDT_OK || B == 0) return st;
@@ -240,6 +269,7 @@ int ddtree_accept_sample_ratio(const float* logits, const float* draft_logits, i
                                uint64_t philox_offset, int32_t* accept_len, int32_t* out_tokens,
                                int32_t* out_nodes, int32_t* bonus, int32_t* dev_status,
                                void* stream) {
+    TraceRange trace("ddtree_accept_sample_ratio");
     int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
                              accept_len, out_tokens, out_nodes, bonus);
     if (st != DDT_OK || B == 0) return st;
@@ -257,6 +287,7 @@ int ddtree_commit_kv(const ddtree_bf16* k_tree, const ddtree_bf16* v_tree, const
                      ddtree_bf16* k_cache, ddtree_bf16* v_cache, int num_pages, int page_size,
                      const int32_t* page_table, int max_pages, const int32_t* ctx_len,
                      int32_t* new_ctx_len, int32_t* dev_status, void* stream) {
+    TraceRange trace("ddtree_commit_kv");
     if (B < 0 || Hkv < 1 || Dh < 1 || page_size < 1 || max_pages < 1 || num_pages < 1)
         return DDT_EINVAL;
     if (N < 1 || N > DDT_MAX_NODES || D < 1 || D > DDT_MAX_DEPTH ||

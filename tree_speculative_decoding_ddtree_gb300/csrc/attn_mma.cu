@@ -318,13 +318,22 @@ attn_combine_kernel(AttnParams p) {
     const bool nn_ok = nn >= 0 && nn <= p.N;
     const int G = p.G;
     const int i = r / G, h = kvh * G + r % G;
+    constexpr int PER = DH / 32;
+    bf16_t* dst = p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * DH + lane * PER;
+    if (!nn_ok) {
+        // A malformed tree: the main kernel flagged it and may have left this
+        // request's partials unwritten, so they are not read. Zeros, lse -inf.
+#pragma unroll
+        for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = 0u;
+        if (p.lse && lane == 0) p.lse[(static_cast<size_t>(b) * p.N + i) * p.Hq + h] = -INFINITY;
+        return;
+    }
     const size_t slot0 = (static_cast<size_t>(b) * p.Hkv + kvh) * p.max_chunks;
     const float2* ml = p.ws_ml + slot0 * p.R + r;            // chunk c at ml[c * R]
     float M = -INFINITY;
     for (int c = lane; c < nchunks; c += 32) M = fmaxf(M, ml[static_cast<size_t>(c) * p.R].x);
     M = warp_max_f(M);
     const float m_use = (M == -INFINITY) ? 0.0f : M;
-    constexpr int PER = DH / 32;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
@@ -353,9 +362,8 @@ attn_combine_kernel(AttnParams p) {
         }
     }
     const float lsum = warp_sum_f(lpart);
-    const bool real = nn_ok && i < nn;
+    const bool real = i < nn;
     const float inv = (real && lsum > 0.0f) ? 1.0f / lsum : 0.0f;
-    bf16_t* dst = p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * DH + lane * PER;
 #pragma unroll
     for (int e = 0; e < PER; e += 2)
         *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);

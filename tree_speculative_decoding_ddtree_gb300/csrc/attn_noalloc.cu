@@ -9,16 +9,24 @@
 //
 // The array is a file-scope __device__ object of kNoAllocScratchBytes. Every
 // GPU on which the library's module is loaded holds it until the process
-// exits. Its device address is looked up once per device, with that device
-// current, by the first call on the device; make that first call before any
-// stream capture. All calls share the one array and its contents persist
+// exits. Its device address is looked up with cudaGetSymbolAddress by the
+// first call on each device (with that device current) and cached together
+// with the id of the CUDA context it belongs to; a later call under another
+// context (after cudaDeviceReset, or under a context the caller made current
+// through the driver API) looks it up again, so a stale address is never
+// used. Make the first call on a device, and the first after a reset, before
+// any stream capture. All calls share the one array and its contents persist
 // between calls: the attention kernels write every scratch word they read
 // within a call, so nothing needs clearing, but two calls that overlap on the
 // GPU (different streams, no ordering between them) race on the array.
 #include <climits>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "trace.h"
 
 namespace ddt {
 void set_last_error(const char* what, cudaError_t e);
@@ -32,9 +40,37 @@ constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+    unsigned long long ctx_id;   // 0: not looked up yet
+    void* ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of g_attn_scratch on the current device (looked up once).
+// Id of the CUDA context current on this thread (0 if none or unavailable).
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_attn_scratch in the current device's current context.
 int scratch_on_current_device(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -44,16 +80,19 @@ int scratch_on_current_device(void** out) {
     }
     if (dev < 0 || dev >= kMaxDevices) return DDT_EINVAL;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    ScratchEntry& ent = g_scratch[dev];
+    const unsigned long long id = current_context_id();
+    if (ent.ctx_id == 0 || id == 0 || id != ent.ctx_id) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        e = cudaGetSymbolAddress(&p, g_attn_scratch);   // also makes the primary context current
         if (e != cudaSuccess || p == nullptr) {
             ddt::set_last_error("cudaGetSymbolAddress(g_attn_scratch)", e);
             return DDT_ECUDA;
         }
-        g_scratch_ptr[dev] = p;
+        ent.ptr = p;
+        ent.ctx_id = current_context_id();   // 0 keeps the next call looking it up again
     }
-    *out = g_scratch_ptr[dev];
+    *out = ent.ptr;
     return DDT_OK;
 }
 
@@ -70,6 +109,7 @@ int tree_verify_attn_noalloc(const ddtree_bf16* q, const ddtree_bf16* k_tree,
                              const uint32_t* vis, const int32_t* n_nodes, int B, int N, int Hq,
                              int Hkv, int Dh, float scale, ddtree_bf16* out, float* lse,
                              int32_t* dev_status, void* stream) {
+    ddt::TraceRange trace("tree_verify_attn_noalloc");
     const long long max_ctx = static_cast<long long>(max_pages) * page_size;
     if (max_pages > 0 && page_size > 0 && max_ctx <= INT_MAX && B > 0) {
         const size_t need = tree_verify_attn_workspace_size(B, N, Hq, Hkv, Dh,

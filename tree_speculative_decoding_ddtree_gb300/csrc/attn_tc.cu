@@ -599,8 +599,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                     uint32_t w[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
-                                                                 __uint_as_float(o[2 * e + 1]) * inv);
+                        __nv_bfloat162 v = __floats2bfloat162_rn(inv != 0.0f ? __uint_as_float(o[2 * e]) * inv : 0.0f,
+                                                                 inv != 0.0f ? __uint_as_float(o[2 * e + 1]) * inv : 0.0f);
                         w[e] = *reinterpret_cast<uint32_t*>(&v);
                     }
 #pragma unroll
@@ -635,8 +635,9 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)   // row stride 36 words: conflict-free 16-byte stores
                         *reinterpret_cast<float4*>(fst + lane * 36 + 4 * e) =
-                            make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                        __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                            good ? make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                               __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]))
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);   // aborted: defined zeros
                     __syncwarp();
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {   // 4 rows x 128 bytes per instruction
@@ -810,8 +811,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 v = __floats2bfloat162_rn(side_o[(d0 + 2 * e) * kMaxSide + sr] * inv,
-                                                             side_o[(d0 + 2 * e + 1) * kMaxSide + sr] * inv);
+                    __nv_bfloat162 v = __floats2bfloat162_rn(inv != 0.0f ? side_o[(d0 + 2 * e) * kMaxSide + sr] * inv : 0.0f,
+                                                             inv != 0.0f ? side_o[(d0 + 2 * e + 1) * kMaxSide + sr] * inv : 0.0f);
                     w[e] = *reinterpret_cast<uint32_t*>(&v);
                 }
                 *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD + d0) =
@@ -822,7 +823,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             } else {
                 float* dst = p.ws_o + (slot * p.R + r) * kD + d0;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) dst[e] = side_o[(d0 + e) * kMaxSide + sr];
+                for (int e = 0; e < 8; ++e) dst[e] = ok ? side_o[(d0 + e) * kMaxSide + sr] : 0.0f;
                 if (d0 == 0) p.ws_ml[slot * p.R + r] = ok ? make_float2(mrun, lt) : make_float2(-INFINITY, 0.0f);
             }
         }

@@ -8,6 +8,7 @@
 #include <new>
 
 #include "common.cuh"
+#include "trace.h"
 
 namespace ddt {
 int cuda_fail(cudaError_t e);
@@ -58,6 +59,7 @@ extern "C" {
 size_t ddtree_step_args_size(void) { return sizeof(ddtree_step_args); }
 
 int ddtree_step_create(const ddtree_step_args* args, ddtree_step** out) {
+    ddt::TraceRange trace("ddtree_step_create");
     if (!out) return DDT_EINVAL;
     *out = nullptr;
     if (!args || args->walk < 0 || args->walk > 2) return DDT_EINVAL;
@@ -97,6 +99,7 @@ int ddtree_step_create(const ddtree_step_args* args, ddtree_step** out) {
 }
 
 int ddtree_step_launch(ddtree_step* step, void* stream) {
+    ddt::TraceRange trace("ddtree_step_launch");
     if (!step || !step->exec) return DDT_EINVAL;
     cudaError_t e = cudaGraphLaunch(step->exec, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DDT_OK : ddt::cuda_fail(e);
