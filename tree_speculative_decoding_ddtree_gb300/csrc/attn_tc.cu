@@ -276,10 +276,10 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             mbar_init(bar_addr(sh.kv_full[s]), 1);
             mbar_init(bar_addr(sh.kv_empty[s]), g.n_side > 0 ? 5 : 1);   // MMA commit + 4 side warps
         }
-        mbar_init(bar_addr(sh.q_tmem), 128 * g.n_main);
+        mbar_init(bar_addr(sh.q_tmem), 4 * g.n_main);   // one arrival per softmax warp
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar_addr(sh.s_full[t]), 1);
-            mbar_init(bar_addr(sh.p_full[t]), 128);
+            mbar_init(bar_addr(sh.p_full[t]), 4);
         }
         mbar_init(bar_addr(sh.o_final), 1);
         for (int k = 0; k < 3; ++k) mbar_init(bar_addr(sh.vfix[k]), 1);
@@ -494,7 +494,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_addr(sh.q_tmem));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(sh.q_tmem));   // one arrival per warp
         }
         const float sc = p.scale_log2;            // > 0 on this path
         float m_ref = -INFINITY;                  // reference max, scaled log2 units
@@ -524,21 +525,22 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                     if (!(c < ti.valid && bit)) raw[c >> 5][c & 31] = 0xFF800000u;   // -inf
                 }
             }
-            // row max of the raw scores (scale > 0 keeps the order), as a tree
+            // row max of the raw scores (scale > 0 keeps the order): four chains of
+            // three-input maxima over 16 columns each, then their maximum
             float mx;
             {
-                float m8[8];
+                float mc[4];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int c0 = 8 * q;
-                    const float a0 = fmaxf(__uint_as_float(raw[c0 >> 5][c0 & 31]), __uint_as_float(raw[(c0 + 1) >> 5][(c0 + 1) & 31]));
-                    const float a1 = fmaxf(__uint_as_float(raw[(c0 + 2) >> 5][(c0 + 2) & 31]), __uint_as_float(raw[(c0 + 3) >> 5][(c0 + 3) & 31]));
-                    const float a2 = fmaxf(__uint_as_float(raw[(c0 + 4) >> 5][(c0 + 4) & 31]), __uint_as_float(raw[(c0 + 5) >> 5][(c0 + 5) & 31]));
-                    const float a3 = fmaxf(__uint_as_float(raw[(c0 + 6) >> 5][(c0 + 6) & 31]), __uint_as_float(raw[(c0 + 7) >> 5][(c0 + 7) & 31]));
-                    m8[q] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+                for (int q = 0; q < 4; ++q) {
+                    const int c0 = 16 * q;
+                    float a = fmaxf(__uint_as_float(raw[c0 >> 5][c0 & 31]), __uint_as_float(raw[(c0 + 1) >> 5][(c0 + 1) & 31]));
+#pragma unroll
+                    for (int k = 2; k < 16; k += 2)
+                        a = fmax3(a, __uint_as_float(raw[(c0 + k) >> 5][(c0 + k) & 31]),
+                                  __uint_as_float(raw[(c0 + k + 1) >> 5][(c0 + k + 1) & 31]));
+                    mc[q] = a;
                 }
-                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
             }
             const float mxs = mx * sc;
             // Raise the reference max of a row when it grows by more than 2^8, and
@@ -565,21 +567,26 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                 m_ref = m_new;
             }
             const float neg_m = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-            // P = 2^(s*scale - m) as bf16 pairs over the first 32 columns of this S buffer
-            float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // P = 2^(s*scale - m) as bf16 pairs over the first 32 columns of this S buffer;
+            // the scaling and the running sums take paired fp32 instructions
+            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(neg_m, neg_m);
+            float2 ls[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(raw[(2 * c) >> 5][(2 * c) & 31]), sc, neg_m));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(raw[(2 * c + 1) >> 5][(2 * c + 1) & 31]), sc, neg_m));
-                ls[c & 3] += p0 + p1;
-                __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+                const float2 x = ffma2(make_float2(__uint_as_float(raw[(2 * c) >> 5][(2 * c) & 31]),
+                                                   __uint_as_float(raw[(2 * c + 1) >> 5][(2 * c + 1) & 31])),
+                                       sc2, nm2);
+                const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                ls[c & 1] = fadd2(ls[c & 1], pe);
+                __nv_bfloat162 v = __floats2bfloat162_rn(pe.x, pe.y);
                 raw[0][c] = *reinterpret_cast<uint32_t*>(&v);
             }
-            l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            l_sum += (ls[0].x + ls[0].y) + (ls[1].x + ls[1].y);
             tmem_st32(tS, raw[0]);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_addr(sh.p_full[t]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_addr(sh.p_full[t]));   // one arrival per warp
         }
         if (active) {
             const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.o_final), 0, abort));

@@ -286,6 +286,28 @@ TC_DEVINL float fast_exp2(float x) {
     return y;
 }
 
+// Paired fp32 arithmetic (one instruction for two lanes of a float2) and the
+// three-input max, which halve the instruction count of the softmax.
+TC_DEVINL float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+TC_DEVINL float2 fadd2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+TC_DEVINL float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte-swizzled
 // region whose rows are 128 bytes and whose base is 1024-byte aligned
 TC_DEVINL uint32_t sw128_offset(int row, int chunk) {
