@@ -172,8 +172,95 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU baseline: the fp64 oracle on a bounded sample, in a fresh process
+# CPU baseline and reference arm: the fp64 oracle on the host cores
 # ---------------------------------------------------------------------------
+
+# One full oracle step over the whole batch: the tree build of every request,
+# the attention of every (request, KV head) slice (all its query heads, over
+# its whole context plus its tree rows) and both walks of every request. The
+# slices and the requests are spread over a pool of worker processes (one per
+# host core; each worker single-threaded), forked after the inputs are made:
+# this process never touches a GPU. `reps` steps are timed one by one.
+ORACLE_POOL_SNIPPET = r"""
+import dataclasses, json, math, multiprocessing as mp, os, platform, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+import ddtree_synth as S
+import oracle as O
+w = S.config({name!r})
+dl, root, _ = S.draft_inputs(w)
+ctx = S.context_lengths(w)
+table, npg = S.paged_layout(w, ctx)
+qkv = S.qkv_tree(w)
+kv = S.kv_cache(w, npg)
+lp, tok = O.draft_topk(dl, w.K)
+tree0 = O.build_tree(lp, tok, root, ctx, w.budget)
+logits = S.target_logits(w, dl, tree0.depth, tree0.n_nodes)
+temp, seed = S.sampling_params(dataclasses.replace(w, temperature=0.7))
+vis0 = O.unpack_vis(tree0.vis, w.N)
+f = O.bf16_to_f64
+G = w.G
+
+def attn_slice(bk):
+    b, kvh = bk
+    L = int(ctx[b])
+    npb = -(-L // w.page_size)
+    pages = table[b, :max(npb, 1)]
+    O.tree_verify_attention(f(qkv["q"][b:b+1, :, kvh*G:(kvh+1)*G]), f(qkv["k_tree"][b:b+1, :, kvh:kvh+1]),
+                            f(qkv["v_tree"][b:b+1, :, kvh:kvh+1]), f(kv["k_cache"][pages][:, :, kvh:kvh+1, :]),
+                            f(kv["v_cache"][pages][:, :, kvh:kvh+1, :]), np.arange(max(npb, 1), dtype=np.int32)[None],
+                            ctx[b:b+1], vis0[b:b+1], tree0.n_nodes[b:b+1], 1 / math.sqrt(w.Dh), w.page_size)
+    return 0
+
+def walks(b):
+    tr = O.build_tree(lp[b:b+1], tok[b:b+1], root[b:b+1], ctx[b:b+1], w.budget)
+    O.accept_greedy(logits[b:b+1], tr, w.D)
+    O.accept_sample(logits[b:b+1], tr, w.D, temp[b:b+1], seed[b:b+1], 0)
+    return 0
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+        out = os.popen("lscpu 2>/dev/null").read()
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+if __name__ == "__main__":
+    cores = {cores} or (os.cpu_count() or 1)
+    tasks = [(b, k) for b in range(w.B) for k in range(w.Hkv)]
+    tasks.sort(key=lambda t: -int(ctx[t[0]]))          # longest slices first
+    steps = []
+    with mp.get_context("fork").Pool(cores) as pool:
+        pool.map(walks, range(min(cores, w.B)))        # workers started and warmed, untimed
+        for rep in range({reps}):
+            t0 = time.perf_counter()
+            r1 = pool.map_async(attn_slice, tasks, chunksize=1)
+            r2 = pool.map_async(walks, range(w.B), chunksize=1)
+            r1.get(); r2.get()
+            steps.append(time.perf_counter() - t0)
+    print(json.dumps(dict(steps=steps, cores=cores, cpu_model=cpu_model(), nproc=os.cpu_count(),
+                          slices=len(tasks))))
+"""
+
+
+def run_oracle_pool(name: str, reps: int, cores: int = 0, timeout: float = 1800):
+    """Full oracle steps on a pool of host cores, in a fresh process with no GPU."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"                                    # one thread per worker process
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = ORACLE_POOL_SNIPPET.format(root=ROOT, name=name, reps=reps, cores=cores)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=timeout)
+    if r.returncode != 0:
+        raise RuntimeError("oracle pool failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
 
 CPU_SNIPPET = r"""
 import dataclasses, json, math, os, sys, time
@@ -229,7 +316,8 @@ print(json.dumps(out))
 
 
 def run_cpu_oracle(name: str, n_slices: int, reps: int = 1):
-    """Run the oracle in a fresh single-threaded process; one dict per repetition."""
+    """One thread: the oracle's build and walks for the whole batch and its
+    attention on a few sampled slices, scaled to the whole step by key count."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
@@ -242,85 +330,22 @@ def run_cpu_oracle(name: str, n_slices: int, reps: int = 1):
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def cpu_baseline_obj(res, n_slices):
-    return {"value": 1.0 / res["step_s"], "unit": "steps/s", "cores": 1, "kind": "oracle",
-            "sample": (f"fp64 numpy oracle, 1 thread: full build + greedy and sampled accept for "
-                       f"all requests, attention on {n_slices} sampled (request, KV head) slices "
-                       f"({res['keys_done']} of {res['total_keys']} context key-heads), scaled to "
-                       f"the whole step by key count")}
+def cpu_baseline_obj(pool, single, n_slices):
+    steps = pool["steps"]
+    step_s = sum(steps) / len(steps)
+    return {"value": 1.0 / step_s, "unit": "steps/s", "cores": pool["cores"], "kind": "oracle",
+            "cpu_model": pool["cpu_model"], "nproc": pool["nproc"],
+            "sample": (f"fp64 numpy oracle, {pool['cores']} worker processes (one per host core, one "
+                       f"thread each): {len(steps)} full steps of the whole batch (build, attention of "
+                       f"all {pool['slices']} (request, KV head) slices over their whole contexts, "
+                       f"greedy and sampled walks), each timed"),
+            "single_thread": {
+                "value": 1.0 / single["step_s"], "unit": "steps/s", "cores": 1,
+                "sample": (f"1 thread: full build + greedy and sampled accept for all requests, attention "
+                           f"on {n_slices} sampled (request, KV head) slices ({single['keys_done']} of "
+                           f"{single['total_keys']} context key-heads), scaled to the whole step by key "
+                           f"count")}}
 
-
-# ---------------------------------------------------------------------------
-# reference arm
-# ---------------------------------------------------------------------------
-
-# Each reference step is a sample sized from a time budget for the whole run:
-# build + greedy + sampled walk for n_req of the B requests (cycled), and the
-# oracle attention of one random (request, KV head) slice over the first n_keys
-# of its context keys plus its tree rows. Both are scaled to the whole step,
-# linearly in requests and in attended keys (context + tree rows, all slices).
-REF_SNIPPET = r"""
-import dataclasses, json, math, sys, time
-sys.path.insert(0, {root!r})
-import numpy as np
-import ddtree_synth as S
-import oracle as O
-w = S.config({name!r})
-reps, budget_s = {reps}, {budget_s}
-dl, root, _ = S.draft_inputs(w)
-ctx = S.context_lengths(w)
-table, npg = S.paged_layout(w, ctx)
-qkv = S.qkv_tree(w)
-kv = S.kv_cache(w, npg)
-lp, tok = O.draft_topk(dl, w.K)
-tree0 = O.build_tree(lp, tok, root, ctx, w.budget)
-logits = S.target_logits(w, dl, tree0.depth, tree0.n_nodes)
-temp, seed = S.sampling_params(dataclasses.replace(w, temperature=0.7))
-f = O.bf16_to_f64
-G = w.G
-vis0 = O.unpack_vis(tree0.vis, w.N)
-all_keys = (int(ctx.sum()) + w.B * w.N) * w.Hkv
-
-def one_request(b):
-    t0 = time.perf_counter()
-    tr = O.build_tree(lp[b:b+1], tok[b:b+1], root[b:b+1], ctx[b:b+1], w.budget)
-    O.accept_greedy(logits[b:b+1], tr, w.D)
-    O.accept_sample(logits[b:b+1], tr, w.D, temp[b:b+1], seed[b:b+1], 0)
-    return time.perf_counter() - t0
-
-def one_slice(b, kvh, n_keys):
-    L = min(int(ctx[b]), n_keys)
-    npb = -(-L // w.page_size)
-    pages = table[b, :max(npb, 1)]
-    t0 = time.perf_counter()
-    kc = f(kv["k_cache"][pages][:, :, kvh:kvh + 1, :]); vc = f(kv["v_cache"][pages][:, :, kvh:kvh + 1, :])
-    O.tree_verify_attention(f(qkv["q"][b:b+1, :, kvh*G:(kvh+1)*G]), f(qkv["k_tree"][b:b+1, :, kvh:kvh+1]),
-                            f(qkv["v_tree"][b:b+1, :, kvh:kvh+1]), kc, vc,
-                            np.arange(max(npb, 1), dtype=np.int32)[None], np.array([L], np.int32),
-                            vis0[b:b+1], tree0.n_nodes[b:b+1], 1 / math.sqrt(w.Dh), w.page_size)
-    return time.perf_counter() - t0, L + w.N
-
-# calibration, untimed: one request, one slice of up to 256 context keys
-t_req = one_request(0)
-t_a, k_a = one_slice(int(np.argmax(ctx)), 0, 256)
-per_step = budget_s / reps
-n_req = max(1, min(w.B, int(0.4 * per_step / max(t_req, 1e-6))))
-n_keys = max(64, min(int(ctx.max()), int(0.4 * per_step * k_a / max(t_a, 1e-6))))
-rng = np.random.default_rng(0)
-out, nb = [], 0
-for rep in range(reps):
-    t_r = 0.0
-    for _ in range(n_req):
-        t_r += one_request(nb % w.B)
-        nb += 1
-    b, kvh = int(rng.integers(w.B)), int(rng.integers(w.Hkv))
-    t_s, keys = one_slice(b, kvh, n_keys)
-    out.append(dict(step_s=t_r * w.B / n_req + t_s * all_keys / keys, n_req=n_req, n_keys=n_keys))
-print(json.dumps(out))
-"""
-
-# seconds of oracle work the reference arm may spend on its K + W steps
-REF_BUDGET_S = 120.0
 
 def mean_context(w):
     """The workload's mean context length in tokens (its seeded lengths), the
@@ -361,19 +386,10 @@ def run_reference(args):
     import ddtree_synth as S
     w = S.config(args.config)
     n_reps = max(args.warmup, 0) + args.steps
-    env = dict(os.environ)
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[k] = "1"
-    env["CUDA_VISIBLE_DEVICES"] = ""
-    code = REF_SNIPPET.format(root=ROOT, name=args.config, reps=n_reps, budget_s=REF_BUDGET_S)
     t0 = time.perf_counter()
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       timeout=3 * REF_BUDGET_S + 900)
+    res = run_oracle_pool(args.config, n_reps)
     elapsed = time.perf_counter() - t0
-    if r.returncode != 0:
-        raise RuntimeError("oracle reference arm failed: " + r.stderr[-2000:])
-    reps = json.loads(r.stdout.strip().splitlines()[-1])
-    per = [r["step_s"] for r in reps[max(args.warmup, 0):]]
+    per = res["steps"][max(args.warmup, 0):]
     step_s = sum(per) / len(per)
     value = 1.0 / step_s
     line = {"metric": METRIC, "value": value, "unit": "steps/s", "impl": "reference",
@@ -382,16 +398,13 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, ddtree_synth)",
             "config": {"workload": WORKLOAD_DESC if args.config == "batched" else args.config,
                        "global_batch": w.B, "seq_len": mean_context(w),
-                       "parallelism": "single process"},
-            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                             "sample": (f"each step: the fp64 oracle's build, greedy and sampled walk for "
-                                        f"{reps[0]['n_req']} of {w.B} requests (cycled) and its attention "
-                                        f"on one random (request, KV head) slice over up to "
-                                        f"{reps[0]['n_keys']} context keys plus the tree rows, scaled to "
-                                        "the whole step linearly in requests and attended keys; the "
-                                        f"sample is sized for at most about {REF_BUDGET_S:.0f} s over the "
-                                        f"{n_reps} steps (capped at the whole batch and the longest "
-                                        "context); 1 thread")},
+                       "parallelism": f"{res['cores']} host processes"},
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": res["cores"], "kind": "oracle",
+                             "cpu_model": res["cpu_model"], "nproc": res["nproc"],
+                             "sample": (f"every step is one full oracle step of the whole batch (no sample, "
+                                        f"no extrapolation): build, attention of all {res['slices']} (request, "
+                                        f"KV head) slices, greedy and sampled walks, over {res['cores']} worker "
+                                        "processes, one thread each")},
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s": elapsed}
@@ -418,10 +431,12 @@ def run_native(args):
 
     w = rank_workload(args.config, rank, world)
 
-    # CPU baseline first, in a fresh process (rank 0, N = 1 only)
-    cpu_res = None
+    # CPU baseline first, in fresh processes (rank 0, N = 1 only): two full
+    # steps on all host cores, and one thread on a sample
+    cpu_pool = cpu_single = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_res = run_cpu_oracle(w.name, args.cpu_sample_slices)[0]
+        cpu_pool = run_oracle_pool(w.name, 2)
+        cpu_single = run_cpu_oracle(w.name, args.cpu_sample_slices)[0]
 
     h = make_host_inputs(w)
     stream = torch.cuda.current_stream(device)
@@ -713,8 +728,8 @@ def run_native(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
         }
-        if cpu_res is not None:
-            line["cpu_baseline"] = cpu_baseline_obj(cpu_res, args.cpu_sample_slices)
+        if cpu_pool is not None:
+            line["cpu_baseline"] = cpu_baseline_obj(cpu_pool, cpu_single, args.cpu_sample_slices)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -243,6 +243,14 @@ size_t tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int Dh,
  *   out_tokens    int32 [B, D+1]  accepted tokens then the bonus; -1 after
  *   out_nodes     int32 [B, D+1]  row 0 then the accepted rows; -1 after
  *   bonus         int32 [B]
+ *   walk_stats    int32 [B, 4]    (nullable) per request: accepted depth
+ *                                 (= accept_len), nodes built (n_nodes as
+ *                                 read), tokens emitted (the commit length:
+ *                                 accepted tokens plus the bonus) and the
+ *                                 children compared without a match.
+ *                                 [Branch] Output Knowledge Created, item 5:
+ *                                 node counts, accepted depths and commit
+ *                                 lengths as debug metrics.
  * Argmax ties go to the lowest index; NaN ranks below every number (an
  * all-NaN row gives 0). Device errors: DDT_DEV_BAD_TREE (walk stops).
  */
@@ -250,7 +258,7 @@ int ddtree_accept_greedy(const float* logits, int V, const int32_t* token,
                          const int32_t* first_child, const int32_t* next_sibling,
                          const int32_t* n_nodes, int B, int N, int D,
                          int32_t* accept_len, int32_t* out_tokens,
-                         int32_t* out_nodes, int32_t* bonus,
+                         int32_t* out_nodes, int32_t* bonus, int32_t* walk_stats,
                          int32_t* dev_status, void* stream);
 
 /*
@@ -275,7 +283,21 @@ int ddtree_accept_greedy(const float* logits, int V, const int32_t* token,
  * (purpose | (offset >> 32) << 8, node, index, offset lo32): purpose 0 =
  * child test (index = child slot, word 0), purpose 1 = Gumbel noise for vocab
  * entry v (index = v >> 2, word v & 3); uniform = ((w >> 8) + 0.5) * 2^-24.
- * Outputs: as ddtree_accept_greedy. Logits must be finite.
+ * Outputs: as ddtree_accept_greedy (walk_stats column 3 counts the child
+ * tests that rejected), plus
+ *   margin_stats  fp32 [B] (nullable): the smallest decision margin on the
+ *                 request's path: |u_j - q(x_j) / R| over the child tests
+ *                 (R = 1 - sum_{i<j} q(x_i)) and, for the bonus, the gap
+ *                 between the best and the runner-up perturbed score
+ *                 logits/T + g; +inf when no decision was taken, NaN for a
+ *                 bad temperature. The kernel's fp32 q values carry a
+ *                 relative error of about 1e-5 at most, which moves a child
+ *                 test's threshold by about 1e-5 / R: a decision whose
+ *                 margin is below that could go the other way in exact
+ *                 arithmetic, and this output lets a caller see such
+ *                 near-threshold requests. [Branch] Output Knowledge
+ *                 Created, item 5 (debug metrics).
+ * Logits must be finite.
  * Device errors: DDT_DEV_BAD_TEMPERATURE (that request emits nothing:
  * accept_len 0, bonus -1), DDT_DEV_BAD_TREE.
  */
@@ -285,6 +307,7 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                          const float* temperature, const uint64_t* seed,
                          uint64_t philox_offset, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
+                         float* margin_stats, int32_t* walk_stats,
                          int32_t* dev_status, void* stream);
 
 /*
@@ -311,7 +334,14 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
  * Randomness: the counters of ddtree_accept_sample (child test: purpose 0,
  * node u, slot j, word 0; Gumbel noise of token v: purpose 1, node u, index
  * v >> 2, word v & 3). A child whose token is outside [0, V) sets
- * DDT_DEV_BAD_TOKEN and is skipped. Device errors as ddtree_accept_sample.
+ * DDT_DEV_BAD_TOKEN and is skipped. margin_stats (nullable, [B]) is the
+ * smallest |U_j - r(x_j) / p(x_j)| over the child tests and the bonus's
+ * top-2 gap of log r + g; walk_stats (nullable, [B, 4]) as
+ * ddtree_accept_sample. Precision: q and p are fp32, c and R fp64, and each
+ * residual max(q - c p, 0) is one fused multiply-add; after rejections the
+ * threshold r(x)/p(x) inherits the fp32 error of q and p amplified by
+ * (1 + c) / R (measured at most 6e-6 (1 + c) / R). Device errors as
+ * ddtree_accept_sample.
  */
 int ddtree_accept_sample_ratio(const float* logits, const float* draft_logits, int V,
                                const int32_t* token, const int32_t* first_child,
@@ -319,8 +349,8 @@ int ddtree_accept_sample_ratio(const float* logits, const float* draft_logits, i
                                int B, int N, int D, const float* temperature,
                                const uint64_t* seed, uint64_t philox_offset,
                                int32_t* accept_len, int32_t* out_tokens,
-                               int32_t* out_nodes, int32_t* bonus,
-                               int32_t* dev_status, void* stream);
+                               int32_t* out_nodes, int32_t* bonus, float* margin_stats,
+                               int32_t* walk_stats, int32_t* dev_status, void* stream);
 
 /*
  * ddtree_commit_kv - append the committed path's K/V to the paged cache.
@@ -428,6 +458,72 @@ size_t ddtree_step_args_size(void);
 int ddtree_step_create(const ddtree_step_args* args, ddtree_step** out);
 int ddtree_step_launch(ddtree_step* step, void* stream);
 void ddtree_step_destroy(ddtree_step* step);
+
+/*
+ * The verify walks for a request split over GPUs by KV head (tensor
+ * parallelism): ddtree_shard_walk_*.
+ *
+ * [Pivot] The Strategic Decision: TP8 (one request spread over the GPUs of a
+ * node). [Arch] Section 1 step 1: the head is vocabulary-parallel, so each
+ * rank holds the logits of its own vocabulary slice [v0, v0 + Vs) only. The
+ * attention of such a request needs no exchange (each rank runs
+ * tree_verify_attn on its own KV heads and their query heads); the walk needs
+ * the argmax, the softmax denominator and the Gumbel-max over the whole
+ * vocabulary at each visited node. These calls split each of those
+ * reductions into a per-rank partial and a merge that every rank performs
+ * identically, so all ranks take the same decisions; between them the
+ * caller exchanges a few words per request (an all-gather over the ranks).
+ * One level of the walk:
+ *
+ *   ddtree_shard_walk_partial   this rank's record per request (36 int32
+ *                               words: the packed argmax key over the slice,
+ *                               the slice's (max, sum of exp(logit/T - max)),
+ *                               the logits of the current node's children
+ *                               that lie in the slice, -inf for the others)
+ *   all-gather of the records   -> [world, B, 36] on every rank
+ *   ddtree_shard_walk_advance   merge in rank order; greedy: follow the child
+ *                               matching the argmax, else emit the bonus;
+ *                               sampled: the child tests of
+ *                               ddtree_accept_sample, else mark the bonus due
+ *   (sampled) ddtree_shard_walk_bonus   this rank's Gumbel-max key over its
+ *                               slice for requests whose bonus is due
+ *   all-gather of the keys      -> [world, B] int64
+ *   (sampled) ddtree_shard_walk_finish  the bonus is the largest key
+ *
+ * D + 1 levels finish every request. ddtree_shard_walk_begin resets the state
+ * and the outputs first. The results equal those of ddtree_accept_greedy /
+ * ddtree_accept_sample on the whole vocabulary: bit for bit for the greedy
+ * walk (the argmax key carries the global index, ties to the lowest), and for
+ * the sampled walk with the same Philox counters (global vocabulary indices)
+ * up to the fp32 rounding of the softmax denominator, which is merged over
+ * ranks instead of over the walk kernel's thread-block cluster.
+ *
+ * Arguments: the tree arrays and outputs as ddtree_accept_greedy (token,
+ * first_child, next_sibling, n_nodes [B, N]; accept_len [B], out_tokens and
+ * out_nodes [B, D+1], bonus [B]); logits_shard fp32 [B, N, Vs] (this rank's
+ * slice of every row); V the whole vocabulary; state int32 [B, 4] (current
+ * node, accepted length, phase, child tests that did not accept) kept on the
+ * device between calls; temperature NULL selects the greedy walk.
+ * Device errors as the unsplit walks.
+ */
+int ddtree_shard_walk_begin(int B, int D, int32_t* state, int32_t* accept_len, int32_t* out_tokens,
+                            int32_t* out_nodes, int32_t* bonus, void* stream);
+int ddtree_shard_walk_partial(const float* logits_shard, int Vs, int v0, int V, const int32_t* token,
+                              const int32_t* first_child, const int32_t* next_sibling,
+                              const int32_t* n_nodes, int B, int N, const float* temperature,
+                              const int32_t* state, int32_t* record, void* stream);
+int ddtree_shard_walk_advance(const int32_t* records, int world, int V, const int32_t* token,
+                              const int32_t* first_child, const int32_t* next_sibling,
+                              const int32_t* n_nodes, int B, int N, int D, const float* temperature,
+                              const uint64_t* seed, uint64_t philox_offset, int32_t* state,
+                              int32_t* accept_len, int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
+                              int32_t* dev_status, void* stream);
+int ddtree_shard_walk_bonus(const float* logits_shard, int Vs, int v0, int V, const int32_t* token,
+                            const int32_t* first_child, const int32_t* next_sibling, const int32_t* n_nodes,
+                            int B, int N, const float* temperature, const uint64_t* seed,
+                            uint64_t philox_offset, const int32_t* state, int64_t* key, void* stream);
+int ddtree_shard_walk_finish(const int64_t* keys, int world, int B, int D, int32_t* state,
+                             int32_t* accept_len, int32_t* out_tokens, int32_t* bonus, void* stream);
 
 /*
  * tree_verify_attn_noalloc - tree_verify_attn without a caller workspace.

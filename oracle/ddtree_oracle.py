@@ -366,6 +366,10 @@ class Accept:
     out_nodes: np.ndarray    # int32 [B, D+1]: root then accepted nodes, -1 after
     bonus: np.ndarray        # int32 [B]
     margin: np.ndarray = None  # fp64 [B]: smallest decision margin (sampling only)
+    rejected: np.ndarray = None  # int32 [B]: child tests that rejected (sampling) or
+    #                              children compared without a match (greedy)
+    margin_scaled: np.ndarray = None  # fp64 [B]: smallest margin / conditioning (sampling only)
+    cond: np.ndarray = None    # fp64 [B]: largest conditioning factor on the path (sampling only)
 
 
 def accept_greedy(logits: np.ndarray, tree: Tree, D: int) -> Accept:
@@ -388,6 +392,7 @@ def accept_greedy(logits: np.ndarray, tree: Tree, D: int) -> Accept:
     toks = np.full((B, D + 1), -1, np.int32)
     nodes = np.full((B, D + 1), -1, np.int32)
     bonus = np.zeros(B, np.int32)
+    rejected = np.zeros(B, np.int32)
     for b in range(B):
         u = 0
         path = []
@@ -398,6 +403,7 @@ def accept_greedy(logits: np.ndarray, tree: Tree, D: int) -> Accept:
                 if int(tree.token[b, c]) == a:
                     match = c
                     break
+                rejected[b] += 1
             if match == -1:
                 bonus[b] = a
                 break
@@ -409,7 +415,7 @@ def accept_greedy(logits: np.ndarray, tree: Tree, D: int) -> Accept:
             toks[b, k] = tree.token[b, c]
             nodes[b, k + 1] = c
         toks[b, len(path)] = bonus[b]
-    return Accept(acc, toks, nodes, bonus)
+    return Accept(acc, toks, nodes, bonus, rejected=rejected)
 
 
 # ----------------------------------------------------------------------------
@@ -517,7 +523,11 @@ def accept_sample(logits: np.ndarray, tree: Tree, D: int, temperature: np.ndarra
 
     ``margin[b]`` is the smallest decision margin on the path:
     |u_j - q(x_j)/R| for each child test and the gap between the two best
-    perturbed scores for the bonus.
+    perturbed scores for the bonus. ``margin_scaled[b]`` divides each child
+    test's margin by its conditioning 1/R (a relative error e in the q values
+    moves the threshold q(x_j)/R by up to about e/R) before taking the
+    minimum; the bonus gap is taken as it is. ``rejected[b]`` counts the
+    child tests that rejected.
     """
     B, N, V = logits.shape
     acc = np.zeros(B, np.int32)
@@ -525,6 +535,9 @@ def accept_sample(logits: np.ndarray, tree: Tree, D: int, temperature: np.ndarra
     nodes = np.full((B, D + 1), -1, np.int32)
     bonus = np.zeros(B, np.int32)
     margin = np.full(B, np.inf)
+    margin_scaled = np.full(B, np.inf)
+    rejected = np.zeros(B, np.int32)
+    cond_max = np.ones(B)
     vidx = np.arange(V, dtype=np.uint64)
     for b in range(B):
         T = float(temperature[b])
@@ -547,10 +560,13 @@ def accept_sample(logits: np.ndarray, tree: Tree, D: int, temperature: np.ndarra
                 if R > 0.0:
                     thr = q[x] / R
                     margin[b] = min(margin[b], abs(uj - thr))
+                    margin_scaled[b] = min(margin_scaled[b], abs(uj - thr) * R)
+                    cond_max[b] = max(cond_max[b], 1.0 / R)
                 if uj * R < q[x]:
                     chosen = c
                     break
                 R -= q[x]
+                rejected[b] += 1
             if chosen != -1:
                 path.append(chosen)
                 u = chosen
@@ -571,6 +587,7 @@ def accept_sample(logits: np.ndarray, tree: Tree, D: int, temperature: np.ndarra
                 if cand.size >= 2:
                     top2 = np.partition(pert[cand], -2)[-2:]
                     margin[b] = min(margin[b], float(top2[1] - top2[0]))
+                    margin_scaled[b] = min(margin_scaled[b], float(top2[1] - top2[0]))
                 bonus[b] = best
             break
         acc[b] = len(path)
@@ -579,7 +596,7 @@ def accept_sample(logits: np.ndarray, tree: Tree, D: int, temperature: np.ndarra
             toks[b, k] = tree.token[b, c]
             nodes[b, k + 1] = c
         toks[b, len(path)] = bonus[b]
-    return Accept(acc, toks, nodes, bonus, margin)
+    return Accept(acc, toks, nodes, bonus, margin, rejected, margin_scaled, cond_max)
 
 
 # ----------------------------------------------------------------------------
@@ -662,7 +679,19 @@ def accept_sample_ratio(logits: np.ndarray, draft_logits: np.ndarray, tree: Tree
     word 0; Gumbel noise of vocab entry v from the Gumbel purpose at index
     v >> 2, word v & 3. ``margin[b]`` is the smallest decision margin on the
     path: |U_j - r(x_j)/p(x_j)| for each child test and the gap between the
-    two best perturbed scores for the bonus.
+    two best perturbed scores for the bonus. ``rejected[b]`` counts the child
+    tests that rejected.
+
+    ``margin_scaled[b]`` divides each margin by its conditioning before the
+    minimum. Written out, the residual after k rejections is
+    r = max(q - C p, 0) / P with C = 0, P = 1 at first and C <- C + P,
+    P <- P * mass at each rejection (tracked here beside the vector r, not
+    used for the decisions). A relative error e in the q and p values moves a
+    child's threshold r(x)/p(x) by up to about e (1 + C) / P, and the
+    perturbed log-score log r(v) of a bonus candidate by about
+    e (q(v) + C p(v)) / (q(v) - C p(v)); the conditioning of a child test is
+    (1 + C) / P, that of the bonus gap the larger of that factor over the two
+    best candidates.
     """
     B, N, V = logits.shape
     acc = np.zeros(B, np.int32)
@@ -670,6 +699,9 @@ def accept_sample_ratio(logits: np.ndarray, draft_logits: np.ndarray, tree: Tree
     nodes = np.full((B, D + 1), -1, np.int32)
     bonus = np.zeros(B, np.int32)
     margin = np.full(B, np.inf)
+    margin_scaled = np.full(B, np.inf)
+    rejected = np.zeros(B, np.int32)
+    cond_max = np.ones(B)
     vidx = np.arange(V, dtype=np.uint64)
 
     def softmax_t(row, T):
@@ -687,6 +719,7 @@ def accept_sample_ratio(logits: np.ndarray, draft_logits: np.ndarray, tree: Tree
         while True:
             q = softmax_t(logits[b, u], T)
             r = q
+            C, P = 0.0, 1.0          # r = max(q - C p, 0) / P (bookkeeping for the conditioning)
             kids = children(tree, b, u) if len(path) < D else []
             chosen = -1
             if kids:
@@ -696,15 +729,20 @@ def accept_sample_ratio(logits: np.ndarray, draft_logits: np.ndarray, tree: Tree
                     uj = float(to_uniform(draw_words(sd, offset, PURPOSE_ACCEPT, u, j)[0]))
                     if p[x] > 0.0:
                         margin[b] = min(margin[b], abs(uj - r[x] / p[x]))
+                        margin_scaled[b] = min(margin_scaled[b], abs(uj - r[x] / p[x]) * P / (1.0 + C))
+                        cond_max[b] = max(cond_max[b], (1.0 + C) / P)
                     if uj * p[x] < r[x]:
                         chosen = c
                         break
+                    rejected[b] += 1
                     res = np.maximum(r - p, 0.0)
                     mass = res.sum()
                     if not mass > 0.0:   # nothing left to renormalise: the bonus comes from q
                         r = q
+                        C, P = 0.0, 1.0
                         break
                     r = res / mass
+                    C, P = C + P, P * mass
             if chosen != -1:
                 path.append(chosen)
                 u = chosen
@@ -720,8 +758,17 @@ def accept_sample_ratio(logits: np.ndarray, draft_logits: np.ndarray, tree: Tree
                 pert = np.log(r[cand]) + g[cand]
                 bonus[b] = int(cand[np.argmax(pert)])
                 if cand.size >= 2:
-                    top2 = np.partition(pert, -2)[-2:]
-                    margin[b] = min(margin[b], float(top2[1] - top2[0]))
+                    order = np.argsort(pert)[-2:]
+                    gap = float(pert[order[1]] - pert[order[0]])
+                    margin[b] = min(margin[b], gap)
+                    if C > 0.0:
+                        pc = softmax_t(draft_logits[b, len(path)], T)
+                        v2 = cand[order]
+                        cond = float(np.max((q[v2] + C * pc[v2]) / (P * r[v2])))   # P r = q - C p
+                    else:
+                        cond = 1.0
+                    margin_scaled[b] = min(margin_scaled[b], gap / cond)
+                    cond_max[b] = max(cond_max[b], cond)
             break
         acc[b] = len(path)
         nodes[b, 0] = 0
@@ -729,4 +776,4 @@ def accept_sample_ratio(logits: np.ndarray, draft_logits: np.ndarray, tree: Tree
             toks[b, k] = tree.token[b, c]
             nodes[b, k + 1] = c
         toks[b, len(path)] = bonus[b]
-    return Accept(acc, toks, nodes, bonus, margin)
+    return Accept(acc, toks, nodes, bonus, margin, rejected, margin_scaled, cond_max)

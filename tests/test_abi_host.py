@@ -8,7 +8,8 @@ import subprocess
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "ddtree.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 from tree_speculative_decoding_ddtree_gb300 import _build  # noqa: E402
 
@@ -21,9 +22,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_four_calls():
@@ -153,14 +156,15 @@ def test_workspace_size(lib):
 
 def walk_args(sample=False, **kw):
     a = dict(logits=FAKE, V=100, token=FAKE, fc=FAKE, ns=FAKE, nn=FAKE, B=2, N=33, D=8,
-             acc=FAKE, toks=FAKE, nodes=FAKE, bonus=FAKE, status=0, stream=0,
+             acc=FAKE, toks=FAKE, nodes=FAKE, bonus=FAKE, margin=0, stats=0, status=0, stream=0,
              temp=FAKE, seed=FAKE, offset=0)
     a.update(kw)
     head = [a[k] for k in ("logits", "V", "token", "fc", "ns", "nn", "B", "N", "D")]
-    tail = [a[k] for k in ("acc", "toks", "nodes", "bonus", "status", "stream")]
-    if sample:
-        return head + [a["temp"], a["seed"], a["offset"]] + tail
-    return head + tail
+    outs = [a[k] for k in ("acc", "toks", "nodes", "bonus")]
+    tail = [a[k] for k in ("status", "stream")]
+    if sample:   # the sampled walks also take the (nullable) margin output
+        return head + [a["temp"], a["seed"], a["offset"]] + outs + [a["margin"], a["stats"]] + tail
+    return head + outs + [a["stats"]] + tail
 
 
 @pytest.mark.parametrize("kw,code", [(dict(V=0), -1), (dict(N=200), -2), (dict(D=0), -2),
@@ -211,3 +215,18 @@ def test_step_create_rejects_before_any_cuda_call(lib):
     assert h.value is None
     lib.ddtree_step_destroy(None)
     assert lib.ddtree_step_launch(None, None) == -1
+
+
+def test_testing_stall_entry_checks_its_limit_on_the_host(lib):
+    # NULL pointers throughout: every outcome is a host-side refusal, so no
+    # kernel can be launched whatever the order of the checks
+    fn = lib.ddtree_testing_attn_stall
+    P, I, F, Z, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, P, I, I, P, I, P, P, P, I, I, I, I, I, F, P, P, P, Z, P, P, U64]
+    args = [None] * 5 + [16, 64, None, 4, None, None, None, 2, 33, 64, 8, 128, 0.08, None, None, None, 0,
+                         None, None]
+    assert "ddtree_testing_attn_stall" in declared_functions()
+    assert fn(*args, 0) == -1                 # no stall asked for
+    assert fn(*args, 2_000_000_000) == -1     # above one second
+    assert fn(*args, 100_000) == -1           # a valid limit, but NULL pointers

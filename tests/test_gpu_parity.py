@@ -2,8 +2,19 @@
 
 Bars: tree structure, masks, positions, fp64 scores, accept lengths and tokens
 bit-exact; attention within max abs 2e-2 and relative L2 1e-2 of the oracle;
-sampled accepts identical given the same Philox counters wherever the
-oracle's decision margin exceeds 1e-4 (fp32 on the GPU vs fp64 in the oracle).
+sampled accepts identical given the same Philox counters on every request
+whose scaled decision margin exceeds 1e-4, with at most two requests per test
+below it.
+
+The sampled walk's bar, derived: the kernel's q(x) = expf((l - M) / T) / Z in
+fp32 carries a relative error of at most about 3 * 2^-24 |l - M| / T (the
+exponent's rounding, |l - M| / T <= 40 here) + 2 ulp (expf) + the fp32 sum Z
+over V (at most about 2e-6), i.e. below 1e-5. A child test compares u with
+q(x_j) / R, R = 1 - sum_{i<j} q(x_i) formed in fp64 from the fp32 q values, so
+the threshold moves by at most about 1e-5 / R; the bonus compares perturbed
+scores logits * (1/T) + g whose error is below 1e-5 as well. The oracle's
+``margin_scaled`` divides each child test's margin by its conditioning 1/R,
+so a scaled margin above 1e-4 is ten times the worst error of that decision.
 """
 import math
 
@@ -354,6 +365,18 @@ def test_accept_greedy_matches_oracle(name):
     assert np.array_equal(g["bonus"].cpu().numpy(), r.bonus)
 
 
+def test_accept_greedy_walk_stats():
+    # accepted depth, nodes built, tokens emitted (accepted + bonus) and the
+    # children compared without a match, per request
+    st = stage(S.config("batched"), attention=False)
+    tree = gpu_tree(st)
+    ws = torch.full((st.w.B, 4), -7, dtype=torch.int32, device="cuda")
+    dd.ddtree_accept_greedy(dev(st.logits), tree, st.w.D, walk_stats=ws)
+    r = O.accept_greedy(st.logits, st.tree, st.w.D)
+    want = np.stack([r.accept_len, st.tree.n_nodes, r.accept_len + 1, r.rejected], axis=1)
+    assert np.array_equal(ws.cpu().numpy(), want)
+
+
 def test_accept_greedy_planted_deep_accepts():
     """Planted logits that agree with the rank-0 chain: the walk reaches full depth."""
     lp, tok = _random_topk(3, 2, 8, 4, V=100)
@@ -397,13 +420,32 @@ def test_accept_greedy_ties_nan_inf_and_odd_vocab():
 # ddtree_accept_sample
 # ---------------------------------------------------------------------------
 
-def compare_sampled(g, r):
-    ok = r.margin > MARGIN
+def compare_sampled(g, r, margin=None, stats=None, n_nodes=None):
+    """Outputs identical on every request whose scaled margin clears the bar;
+    the optional margin and stats outputs checked on the same requests (the
+    margin within 1e-5 times the path's largest conditioning, the fp32 bound
+    of any one decision). Returns the number of requests below the bar."""
+    ok = r.margin_scaled > MARGIN
     for key, ref in (("accept_len", r.accept_len), ("out_tokens", r.out_tokens),
                      ("out_nodes", r.out_nodes), ("bonus", r.bonus)):
         got = g[key].cpu().numpy()
         assert np.array_equal(got[ok], ref[ok]), key
+    if margin is not None:
+        m = margin.cpu().numpy().astype(np.float64)
+        fin = ok & np.isfinite(r.margin)
+        assert np.all(np.abs(m[fin] - r.margin[fin]) <= 1e-5 * r.cond[fin] + 1e-6), \
+            np.max(np.abs(m[fin] - r.margin[fin]))
+        assert np.all(np.isinf(m[ok & np.isinf(r.margin)]))
+    if stats is not None:
+        emitted = r.accept_len + (r.bonus >= 0)
+        want = np.stack([r.accept_len, n_nodes, emitted, r.rejected], axis=1)
+        assert np.array_equal(stats.cpu().numpy()[ok], want[ok])
     return int((~ok).sum())
+
+
+def walk_extras(B):
+    return (torch.full((B,), -1.0, dtype=torch.float32, device="cuda"),
+            torch.full((B, 4), -7, dtype=torch.int32, device="cuda"))
 
 
 def test_accept_sample_temperature_config():
@@ -411,12 +453,13 @@ def test_accept_sample_temperature_config():
     temp, seed = S.sampling_params(st.w)
     tree = gpu_tree(st)
     s = status()
+    m, ws = walk_extras(st.w.B)
     g = dd.ddtree_accept_sample(dev(st.logits), tree, st.w.D, dev(temp), dev(seed), 1234,
-                                dev_status=s)
+                                dev_status=s, margin_stats=m, walk_stats=ws)
     r = O.accept_sample(st.logits, st.tree, st.w.D, temp, seed, 1234)
     torch.cuda.synchronize()
     assert int(s.item()) == 0
-    assert compare_sampled(g, r) <= 1
+    assert compare_sampled(g, r, m, ws, st.tree.n_nodes) <= 2
 
 
 @pytest.mark.parametrize("T,offset", [(0.3, 0), (1.0, 5), (2.5, (7 << 32) + 3)])
@@ -428,9 +471,11 @@ def test_accept_sample_many_seeds(T, offset):
     temp = np.full(B, T, np.float32)
     seed = np.arange(B, dtype=np.uint64) * np.uint64(2654435761) + np.uint64(1)
     tree = gpu_tree(st)
-    g = dd.ddtree_accept_sample(dev(st.logits), tree, w.D, dev(temp), dev(seed), offset)
+    m, ws = walk_extras(B)
+    g = dd.ddtree_accept_sample(dev(st.logits), tree, w.D, dev(temp), dev(seed), offset,
+                                margin_stats=m, walk_stats=ws)
     r = O.accept_sample(st.logits, st.tree, w.D, temp, seed, offset)
-    assert compare_sampled(g, r) <= 2
+    assert compare_sampled(g, r, m, ws, st.tree.n_nodes) <= 2
 
 
 def test_accept_sample_low_temperature_equals_greedy():
@@ -447,8 +492,10 @@ def test_accept_sample_bad_temperature_flagged():
     st = stage(S.config("tiny"), attention=False)
     tree = gpu_tree(st)
     s = status()
+    m, ws = walk_extras(1)
     g = dd.ddtree_accept_sample(dev(st.logits), tree, st.w.D, dev(np.zeros(1, np.float32)),
-                                dev(np.array([1], np.uint64)), 0, dev_status=s)
+                                dev(np.array([1], np.uint64)), 0, dev_status=s, margin_stats=m, walk_stats=ws)
     torch.cuda.synchronize()
     assert int(s.item()) & 8
     assert int(g["accept_len"][0]) == 0 and int(g["bonus"][0]) == -1
+    assert math.isnan(float(m[0])) and ws[0].tolist() == [0, int(st.tree.n_nodes[0]), 0, 0]

@@ -71,7 +71,7 @@ def load_library(path: Optional[str] = None):
     lib.ddtree_step_destroy.restype = None
     lib.ddtree_step_destroy.argtypes = [P]
     lib.ddtree_accept_sample_ratio.restype = I
-    lib.ddtree_accept_sample_ratio.argtypes = [P, P, I, P, P, P, P, I, I, I, P, P, U64, P, P, P, P, P, P]
+    lib.ddtree_accept_sample_ratio.argtypes = [P, P, I, P, P, P, P, I, I, I, P, P, U64, P, P, P, P, P, P, P, P]
     lib.ddtree_build.restype = I
     lib.ddtree_build.argtypes = [P] * 4 + [I] * 4 + [P] * 10 + [P, P]
     lib.tree_verify_attn.restype = I
@@ -80,9 +80,9 @@ def load_library(path: Optional[str] = None):
     lib.tree_verify_attn_workspace_size.restype = Z
     lib.tree_verify_attn_workspace_size.argtypes = [I, I, I, I, I, I]
     lib.ddtree_accept_greedy.restype = I
-    lib.ddtree_accept_greedy.argtypes = [P, I, P, P, P, P, I, I, I, P, P, P, P, P, P]
+    lib.ddtree_accept_greedy.argtypes = [P, I, P, P, P, P, I, I, I, P, P, P, P, P, P, P]
     lib.ddtree_accept_sample.restype = I
-    lib.ddtree_accept_sample.argtypes = [P, I, P, P, P, P, I, I, I, P, P, U64, P, P, P, P, P, P]
+    lib.ddtree_accept_sample.argtypes = [P, I, P, P, P, P, I, I, I, P, P, U64, P, P, P, P, P, P, P, P]
     if path is None:
         _lib = lib
     return lib
@@ -257,8 +257,12 @@ def _walk_outputs(B, D, device, out):
 
 
 def ddtree_accept_greedy(logits: torch.Tensor, tree: TreeBuffers, D: int, out=None,
-                         dev_status: Optional[torch.Tensor] = None, stream=None):
-    """Greedy verify walk (see ``ddtree_accept_greedy`` in include/ddtree.h)."""
+                         dev_status: Optional[torch.Tensor] = None, stream=None,
+                         walk_stats: Optional[torch.Tensor] = None):
+    """Greedy verify walk (see ``ddtree_accept_greedy`` in include/ddtree.h).
+
+    ``walk_stats`` (optional int32 ``[B, 4]``) receives accepted depth, nodes
+    built, tokens emitted and children compared without a match."""
     lib = load_library()
     B, N, V = logits.shape
     o = _walk_outputs(B, D, logits.device, out)
@@ -272,6 +276,7 @@ def ddtree_accept_greedy(logits: torch.Tensor, tree: TreeBuffers, D: int, out=No
         _ptr(o["out_tokens"], torch.int32, "out_tokens", (B, D + 1)),
         _ptr(o["out_nodes"], torch.int32, "out_nodes", (B, D + 1)),
         _ptr(o["bonus"], torch.int32, "bonus", (B,)),
+        _ptr(walk_stats, torch.int32, "walk_stats", (B, 4)),
         _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
     _check(st, "ddtree_accept_greedy")
     return o
@@ -279,10 +284,13 @@ def ddtree_accept_greedy(logits: torch.Tensor, tree: TreeBuffers, D: int, out=No
 
 def ddtree_accept_sample_ratio(logits: torch.Tensor, draft_logits: torch.Tensor, tree: TreeBuffers,
                                D: int, temperature: torch.Tensor, seed: torch.Tensor, philox_offset: int,
-                               out=None, dev_status: Optional[torch.Tensor] = None, stream=None):
+                               out=None, dev_status: Optional[torch.Tensor] = None, stream=None,
+                               margin_stats: Optional[torch.Tensor] = None,
+                               walk_stats: Optional[torch.Tensor] = None):
     """Temperature walk with the draft-ratio rule (see ``ddtree_accept_sample_ratio`` in
     include/ddtree.h). ``draft_logits`` fp32 ``[B, D, V]``; ``seed`` int64 ``[B]``
-    holding the uint64 seeds."""
+    holding the uint64 seeds; optional ``margin_stats`` fp32 ``[B]`` and
+    ``walk_stats`` int32 ``[B, 4]``."""
     lib = load_library()
     B, N, V = logits.shape
     o = _walk_outputs(B, D, logits.device, out)
@@ -299,6 +307,8 @@ def ddtree_accept_sample_ratio(logits: torch.Tensor, draft_logits: torch.Tensor,
         _ptr(o["out_tokens"], torch.int32, "out_tokens", (B, D + 1)),
         _ptr(o["out_nodes"], torch.int32, "out_nodes", (B, D + 1)),
         _ptr(o["bonus"], torch.int32, "bonus", (B,)),
+        _ptr(margin_stats, torch.float32, "margin_stats", (B,)),
+        _ptr(walk_stats, torch.int32, "walk_stats", (B, 4)),
         _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
     _check(st, "ddtree_accept_sample_ratio")
     return o
@@ -334,10 +344,14 @@ def ddtree_commit_kv(k_tree: torch.Tensor, v_tree: torch.Tensor, accept: dict,
 
 def ddtree_accept_sample(logits: torch.Tensor, tree: TreeBuffers, D: int,
                          temperature: torch.Tensor, seed: torch.Tensor, philox_offset: int,
-                         out=None, dev_status: Optional[torch.Tensor] = None, stream=None):
+                         out=None, dev_status: Optional[torch.Tensor] = None, stream=None,
+                         margin_stats: Optional[torch.Tensor] = None,
+                         walk_stats: Optional[torch.Tensor] = None):
     """Temperature verify walk (see ``ddtree_accept_sample`` in include/ddtree.h).
 
-    ``seed`` is int64 on the device, read as uint64 bits.
+    ``seed`` is int64 on the device, read as uint64 bits. Optional
+    ``margin_stats`` fp32 ``[B]`` receives each request's smallest decision
+    margin and ``walk_stats`` int32 ``[B, 4]`` its walk statistics.
     """
     lib = load_library()
     B, N, V = logits.shape
@@ -354,6 +368,8 @@ def ddtree_accept_sample(logits: torch.Tensor, tree: TreeBuffers, D: int,
         _ptr(o["out_tokens"], torch.int32, "out_tokens", (B, D + 1)),
         _ptr(o["out_nodes"], torch.int32, "out_nodes", (B, D + 1)),
         _ptr(o["bonus"], torch.int32, "bonus", (B,)),
+        _ptr(margin_stats, torch.float32, "margin_stats", (B,)),
+        _ptr(walk_stats, torch.int32, "walk_stats", (B, 4)),
         _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
     _check(st, "ddtree_accept_sample")
     return o

@@ -33,6 +33,7 @@ accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
     __shared__ TreeRows tr;
     __shared__ int s_next;
     __shared__ int s_len;
+    __shared__ int s_rej;
     const uint32_t rank = cluster_rank();
     const bool writer = rank == 0;
     const int b = static_cast<int>(blockIdx.x) / kCluster;
@@ -43,12 +44,13 @@ accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
     if (writer)
         for (int k = threadIdx.x; k <= D; k += kWalkThreads) { toks[k] = -1; nodes[k] = -1; }
     stage_tree(tr, token, first_child, next_sibling, tb, N);
-    int nn = n_nodes[b];
+    const int nn_read = n_nodes[b];
+    int nn = nn_read;
     if (nn < 1 || nn > N) {
         if (threadIdx.x == 0 && writer) report(dev_status, DDT_DEV_BAD_TREE);
         nn = nn < 1 ? 1 : N;
     }
-    if (threadIdx.x == 0) s_len = 0;
+    if (threadIdx.x == 0) { s_len = 0; s_rej = 0; }
     __syncthreads();
     if (threadIdx.x == 0 && writer) nodes[0] = 0;
     int u = 0;
@@ -66,6 +68,7 @@ accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
                     break;
                 }
                 if (tr.tok[c] == static_cast<int32_t>(a)) { match = c; break; }
+                ++s_rej;
                 c = tr.ns[c];
             }
             const int len = s_len;
@@ -83,6 +86,7 @@ accept_greedy_kernel(const float* __restrict__ logits, int V, bool vec4,
                 toks[len] = static_cast<int32_t>(a);
                 o.bonus[b] = static_cast<int32_t>(a);
                 o.accept_len[b] = len;
+                write_stats(o, b, len, nn_read, len + 1, s_rej);
             }
             s_next = match;
         }
@@ -103,8 +107,10 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     __shared__ unsigned long long scratch_u[32];
     __shared__ float scratch_m[32];
     __shared__ float scratch_z[32];
+    __shared__ float2 scratch_g[32];
     __shared__ float2 part_ms[2];               // this CTA's partial (max, sum), by level parity
     __shared__ unsigned long long part_g;       // this CTA's partial Gumbel-max (bonus)
+    __shared__ float2 part_gap;                 // its two best perturbed scores (margin output only)
     __shared__ TreeRows tr;
     __shared__ int s_kid_tok[kMaxKids];
     __shared__ int s_kid_node[kMaxKids];
@@ -115,6 +121,8 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     __shared__ int s_nkids;
     __shared__ int s_next;
     __shared__ int s_len;
+    __shared__ int s_rej;
+    __shared__ float s_margin;
     const uint32_t rank = cluster_rank();
     const bool writer = rank == 0;
     const int b = static_cast<int>(blockIdx.x) / kCluster;
@@ -125,7 +133,8 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     if (writer)
         for (int k = threadIdx.x; k <= D; k += kWalkThreads) { toks[k] = -1; nodes[k] = -1; }
     stage_tree(tr, token, first_child, next_sibling, tb, N);
-    int nn = n_nodes[b];
+    const int nn_read = n_nodes[b];
+    int nn = nn_read;
     if (nn < 1 || nn > N) {
         if (threadIdx.x == 0 && writer) report(dev_status, DDT_DEV_BAD_TREE);
         nn = nn < 1 ? 1 : N;
@@ -137,6 +146,8 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
             report(dev_status, DDT_DEV_BAD_TEMPERATURE);
             o.accept_len[b] = 0;
             o.bonus[b] = -1;
+            if (o.margin) o.margin[b] = NAN;
+            write_stats(o, b, 0, nn_read, 0, 0);
         }
         return;
     }
@@ -147,6 +158,8 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     const uint32_t off_hi8 = static_cast<uint32_t>(offset >> 32) << 8;
     if (threadIdx.x == 0) {
         s_len = 0;
+        s_rej = 0;
+        s_margin = INFINITY;
         if (writer) nodes[0] = 0;
     }
     int u = 0;
@@ -246,8 +259,11 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
             int match = -1;
             double R = 1.0;
             for (int j = 0; j < nk; ++j) {
+                if (o.margin && R > 0.0)   // fp32 is enough for the report; no fp64 divide on the walk's path
+                    s_margin = fminf(s_margin, fabsf(static_cast<float>(s_u[j]) - s_q[j] / static_cast<float>(R)));
                 if (s_u[j] * R < static_cast<double>(s_q[j])) { match = s_kid_node[j]; break; }
                 R -= static_cast<double>(s_q[j]);
+                ++s_rej;
             }
             const int len = s_len;
             if (match != -1 && len >= D) {
@@ -267,7 +283,10 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         const int nxt = s_next;
         if (nxt != -1) { u = nxt; continue; }
         // bonus: Gumbel-max over this CTA's slice, tokens that are not children of u
+        // (with a margin output, the two best scores too: their gap is the draw's margin)
+        const bool want_gap = o.margin != nullptr;
         unsigned long long best = 0ull;
+        Gap2 gap{-INFINITY, -INFINITY};
         const int g0 = vec4 ? sl.g0 : (sl.g0 >> 2), g1 = vec4 ? sl.g1 : ((sl.g1 + 3) >> 2);
 #pragma unroll 2
         for (int x = g0 + static_cast<int>(threadIdx.x); x < g1; x += kWalkThreads) {
@@ -292,12 +311,17 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
                 if (kid) continue;
                 const float g = -logf(neg_log_uniform(ws[e]));
                 const float sc = f[e] * inv_t + g;
-                const unsigned long long p = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
-                best = best > p ? best : p;
+                const unsigned long long pk = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
+                best = best > pk ? best : pk;
+                if (want_gap) gap2_add(gap, sc);
             }
         }
         best = block_reduce(best, scratch_u, MaxU64(), 0ull);
-        if (threadIdx.x == 0) part_g = best;
+        if (want_gap) gap = block_gap2(gap, scratch_g);
+        if (threadIdx.x == 0) {
+            part_g = best;
+            part_gap = make_float2(gap.top, gap.sec);
+        }
         cluster_barrier();
         if (threadIdx.x == 0 && writer) {
             const unsigned long long all = cluster_max_u64(&part_g);
@@ -306,6 +330,8 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
             toks[len] = a;
             o.bonus[b] = a;
             o.accept_len[b] = len;
+            if (want_gap) o.margin[b] = fminf(s_margin, cluster_gap(&part_gap));
+            write_stats(o, b, len, nn_read, len + (a >= 0 ? 1 : 0), s_rej);
         }
         break;
     }
@@ -316,9 +342,10 @@ cudaError_t launch_accept_greedy(const float* logits, int V, const int32_t* toke
                                  const int32_t* first_child, const int32_t* next_sibling,
                                  const int32_t* n_nodes, int B, int N, int D,
                                  int32_t* accept_len, int32_t* out_tokens, int32_t* out_nodes,
-                                 int32_t* bonus, int32_t* dev_status, cudaStream_t stream) {
+                                 int32_t* bonus, int32_t* walk_stats, int32_t* dev_status,
+                                 cudaStream_t stream) {
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
-    WalkOut o{accept_len, out_tokens, out_nodes, bonus};
+    WalkOut o{accept_len, out_tokens, out_nodes, bonus, nullptr, walk_stats};
     accept_greedy_kernel<<<B * kCluster, kWalkThreads, 0, stream>>>(logits, V, vec4, token, first_child,
                                                                     next_sibling, n_nodes, N, D, o, dev_status);
     return cudaGetLastError();
@@ -329,9 +356,10 @@ cudaError_t launch_accept_sample(const float* logits, int V, const int32_t* toke
                                  const int32_t* n_nodes, int B, int N, int D,
                                  const float* temperature, const uint64_t* seed, uint64_t offset,
                                  int32_t* accept_len, int32_t* out_tokens, int32_t* out_nodes,
-                                 int32_t* bonus, int32_t* dev_status, cudaStream_t stream) {
+                                 int32_t* bonus, float* margin_stats, int32_t* walk_stats,
+                                 int32_t* dev_status, cudaStream_t stream) {
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
-    WalkOut o{accept_len, out_tokens, out_nodes, bonus};
+    WalkOut o{accept_len, out_tokens, out_nodes, bonus, margin_stats, walk_stats};
     accept_sample_kernel<<<B * kCluster, kWalkThreads, 0, stream>>>(logits, V, vec4, token, first_child,
                                                                     next_sibling, n_nodes, N, D, temperature,
                                                                     seed, offset, o, dev_status);

@@ -15,6 +15,14 @@
 // U_j * p(x) < r(x). The bonus is the Gumbel-max of log max(q - c p, 0); if
 // the residual has no mass left the bonus is drawn from q.
 //
+// Precision: q and p are fp32 (expf over the row, fp32 sums); c and R are
+// fp64 scalars (R summed in fp64 across the threads' fp32 partials), and
+// every residual q - c p is formed with one fused multiply-add on the high
+// part of c (the low part's product subtracted after), so the subtraction
+// adds no rounding beyond that of its result. What remains is the fp32 error
+// of q and p themselves, which a rejection chain amplifies by (1 + c) / R:
+// that conditioning is the problem's, not the formula's.
+//
 // Same layout as the other walks: one 8-CTA cluster per request; every pass
 // over a row is split into the CTAs' slices and combined through distributed
 // shared memory in rank order, so every CTA holds identical values and takes
@@ -85,18 +93,25 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                     const uint64_t* __restrict__ seed, uint64_t offset, WalkOut o, int32_t* dev_status) {
     __shared__ unsigned long long scratch_u[32];
     __shared__ float scratch_a[32], scratch_b[32];
+    __shared__ float2 scratch_g[32];
     __shared__ float4 part_s[2];                // (max, sum) of the target and the draft row, by round
-    __shared__ float part_r[2];                 // residual mass, by round
+    __shared__ double part_r[2];                // residual mass, by round (the cluster sums it in fp64)
     __shared__ unsigned long long part_g[2];    // Gumbel-max, by round
+    __shared__ float2 part_gap[2];              // two best perturbed scores, by round (margin output only)
     __shared__ TreeRows tr;
     __shared__ int s_kid_tok[kMaxKids];
     __shared__ int s_kid_node[kMaxKids];
     __shared__ float s_kid_l[kMaxKids];         // target logit of the child's token
     __shared__ float s_kid_d[kMaxKids];         // draft logit of the child's token
     __shared__ double s_u[kMaxKids];
-    __shared__ float s_mq, s_zq, s_mp, s_zp, s_R;
+    __shared__ float s_mq, s_zq, s_mp, s_zp;
+    __shared__ double s_R, s_c;                 // thread 0's fp64 residual mass and offset
+    __shared__ float s_chi, s_clo;              // c = s_chi + s_clo for every thread
+    __shared__ int s_rpos;                      // the residual still has mass
+    __shared__ float s_margin;
     __shared__ unsigned long long s_best;
-    __shared__ int s_nkids, s_state, s_next, s_len;
+    __shared__ float s_gap;
+    __shared__ int s_nkids, s_state, s_next, s_len, s_rej;
     const uint32_t rank = cluster_rank();
     const bool writer = rank == 0;
     const int b = static_cast<int>(blockIdx.x) / kCluster;
@@ -107,7 +122,8 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
     if (writer)
         for (int k = threadIdx.x; k <= D; k += kWalkThreads) { toks[k] = -1; nodes[k] = -1; }
     stage_tree(tr, token, first_child, next_sibling, tb, N);
-    int nn = n_nodes[b];
+    const int nn_read = n_nodes[b];
+    int nn = nn_read;
     if (nn < 1 || nn > N) {
         if (threadIdx.x == 0 && writer) report(dev_status, DDT_DEV_BAD_TREE);
         nn = nn < 1 ? 1 : N;
@@ -119,6 +135,8 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
             report(dev_status, DDT_DEV_BAD_TEMPERATURE);
             o.accept_len[b] = 0;
             o.bonus[b] = -1;
+            if (o.margin) o.margin[b] = NAN;
+            write_stats(o, b, 0, nn_read, 0, 0);
         }
         return;
     }
@@ -129,6 +147,8 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
     const uint32_t off_hi8 = static_cast<uint32_t>(offset >> 32) << 8;
     if (threadIdx.x == 0) {
         s_len = 0;
+        s_rej = 0;
+        s_margin = INFINITY;
         if (writer) nodes[0] = 0;
     }
     int round = 0;   // cluster reductions so far: partial slots alternate by its parity
@@ -202,12 +222,21 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                 ap = merge_ms(ap, MaxSum{p2.x, p2.y}, inv_t);
             }
             s_mq = aq.m; s_zq = aq.z; s_mp = ap.m; s_zp = ap.z;
+            s_c = 0.0;
+            s_R = 1.0;
         }
         ++round;
         __syncthreads();
         const float Mq = s_mq, rZq = 1.0f / s_zq, Mp = s_mp, rZp = nk > 0 ? 1.0f / s_zp : 0.0f;
-        // children in rank order against the residual max(q - c p, 0) / R
-        float c = 0.0f, R = 1.0f;
+        // children in rank order against the residual max(q - c p, 0) / R; thread 0
+        // keeps c and R in fp64 and hands every thread c = c_hi + c_lo, the
+        // residuals take fmaf on c_hi
+        float c_hi = 0.0f, c_lo = 0.0f;
+        auto resid = [&](float qv, float pv) { return fmaxf(fmaf(-c_hi, pv, qv) - c_lo * pv, 0.0f); };
+        // the residual of vocabulary entry v from its target and draft logits
+        auto qp = [&](float l, float d) {
+            return resid(expf((l - Mq) * inv_t) * rZq, expf((d - Mp) * inv_t) * rZp);
+        };
         int match = -1;
         for (int j = 0; j < nk; ++j) {
             if (threadIdx.x == 0) {
@@ -219,8 +248,17 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                 } else {
                     const float qx = expf((s_kid_l[j] - Mq) * inv_t) * rZq;
                     const float px = expf((s_kid_d[j] - Mp) * inv_t) * rZp;
-                    const float rx = fmaxf(qx - c * px, 0.0f) / R;
-                    st = s_u[j] * static_cast<double>(px) < static_cast<double>(rx) ? kAccept : kReject;
+                    const double R = s_R;
+                    const float ru = resid(qx, px);   // R r(x): the test U p(x) < r(x) without a divide
+                    if (o.margin && px > 0.0f)        // fp32 is enough for the report
+                        s_margin = fminf(s_margin, fabsf(static_cast<float>(s_u[j]) - ru / (px * static_cast<float>(R))));
+                    st = s_u[j] * static_cast<double>(px) * R < static_cast<double>(ru) ? kAccept : kReject;
+                    if (st == kReject) {
+                        s_c += R;
+                        s_chi = static_cast<float>(s_c);
+                        s_clo = static_cast<float>(s_c - static_cast<double>(s_chi));
+                    }
+                    if (st == kReject) ++s_rej;
                 }
                 s_state = st;
             }
@@ -229,38 +267,36 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
             __syncthreads();   // every thread has read s_state before thread 0 writes it again
             if (st == kAccept) { match = s_kid_node[j]; break; }
             if (st == kSkip) continue;
-            c += R;
+            c_hi = s_chi;
+            c_lo = s_clo;
             // the residual's mass for the next test, or to confirm the bonus has one
             float part = 0.0f;
-            auto resid = [&](float l, float d) {
-                return fmaxf(expf((l - Mq) * inv_t) * rZq - c * (expf((d - Mp) * inv_t) * rZp), 0.0f);
-            };
             if (vec4) {
                 const float4* r4 = reinterpret_cast<const float4*>(row);
                 const float4* d4 = reinterpret_cast<const float4*>(drow);
-#pragma unroll 2
+#pragma unroll 1   // each thread takes about two groups per pass; unrolling only adds registers
                 for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads) {
                     const float4 f = __ldg(r4 + x), g = __ldg(d4 + x);
-                    part += resid(f.x, g.x) + resid(f.y, g.y) + resid(f.z, g.z) + resid(f.w, g.w);
+                    part += qp(f.x, g.x) + qp(f.y, g.y) + qp(f.z, g.z) + qp(f.w, g.w);
                 }
             } else {
                 for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads)
-                    part += resid(__ldg(row + v), __ldg(drow + v));
+                    part += qp(__ldg(row + v), __ldg(drow + v));
             }
             part = block_sum_f(part, scratch_a);
-            if (threadIdx.x == 0) part_r[round & 1] = part;
+            if (threadIdx.x == 0) part_r[round & 1] = static_cast<double>(part);
             cluster_barrier();
             if (threadIdx.x == 0) {   // in rank order: the same sum in every CTA
-                float all = 0.0f;
+                double all = 0.0;
 #pragma unroll
-                for (int r = 0; r < kCluster; ++r) all += ld_cluster_f32(cluster_addr(&part_r[round & 1], r));
+                for (int r = 0; r < kCluster; ++r) all += ld_cluster_f64(cluster_addr(&part_r[round & 1], r));
                 s_R = all;
+                s_rpos = all > 0.0;
             }
             ++round;
             __syncthreads();
-            R = s_R;
-            if (!(R > 0.0f)) {   // no residual mass left: the bonus comes from q
-                c = 0.0f;
+            if (!s_rpos) {   // no residual mass left: the bonus comes from q
+                c_hi = c_lo = 0.0f;
                 break;
             }
         }
@@ -279,8 +315,11 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
         if (s_next != -1) { u = s_next; continue; }
         // bonus: Gumbel-max of log max(q - c p, 0) over this CTA's slice; if no
         // token keeps residual mass, once more with c = 0 (from q)
+        const bool want_gap = o.margin != nullptr;
         for (;;) {
+        const bool from_resid = c_hi > 0.0f;   // else from q
         unsigned long long best = 0ull;
+        Gap2 gap{-INFINITY, -INFINITY};
         const int g0 = vec4 ? sl.g0 : (sl.g0 >> 2), g1 = vec4 ? sl.g1 : ((sl.g1 + 3) >> 2);
 #pragma unroll 2
         for (int x = g0 + static_cast<int>(threadIdx.x); x < g1; x += kWalkThreads) {
@@ -291,7 +330,7 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
             if (vec4) {
                 const float4 t4 = __ldg(reinterpret_cast<const float4*>(row) + x);
                 f[0] = t4.x; f[1] = t4.y; f[2] = t4.z; f[3] = t4.w;
-                if (c > 0.0f) {
+                if (from_resid) {
                     const float4 d4 = __ldg(reinterpret_cast<const float4*>(drow) + x);
                     d[0] = d4.x; d[1] = d4.y; d[2] = d4.z; d[3] = d4.w;
                 }
@@ -300,7 +339,7 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                 for (int e = 0; e < 4; ++e) {
                     const int v = 4 * x + e;
                     f[e] = v < V ? __ldg(row + v) : 0.0f;
-                    d[e] = (v < V && c > 0.0f) ? __ldg(drow + v) : 0.0f;
+                    d[e] = (v < V && from_resid) ? __ldg(drow + v) : 0.0f;
                 }
             }
 #pragma unroll
@@ -308,26 +347,34 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                 const int v = 4 * x + e;
                 if (v >= V || (!vec4 && (v < sl.g0 || v >= sl.g1))) continue;
                 float sc;
-                if (c > 0.0f) {
-                    const float r = expf((f[e] - Mq) * inv_t) * rZq - c * (expf((d[e] - Mp) * inv_t) * rZp);
+                if (from_resid) {
+                    const float r = qp(f[e], d[e]);
                     if (!(r > 0.0f)) continue;
                     sc = logf(r);
                 } else {
                     sc = (f[e] - Mq) * inv_t;   // log q up to a constant
                 }
                 sc += -logf(neg_log_uniform(ws[e]));
-                const unsigned long long p = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
-                best = best > p ? best : p;
+                const unsigned long long pk = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
+                best = best > pk ? best : pk;
+                if (want_gap) gap2_add(gap, sc);
             }
         }
         best = block_reduce(best, scratch_u, MaxU64(), 0ull);
-        if (threadIdx.x == 0) part_g[round & 1] = best;
+        if (want_gap) gap = block_gap2(gap, scratch_g);
+        if (threadIdx.x == 0) {
+            part_g[round & 1] = best;
+            part_gap[round & 1] = make_float2(gap.top, gap.sec);
+        }
         cluster_barrier();
-        if (threadIdx.x == 0) s_best = cluster_max_u64(&part_g[round & 1]);
+        if (threadIdx.x == 0) {
+            s_best = cluster_max_u64(&part_g[round & 1]);
+            if (want_gap) s_gap = cluster_gap(&part_gap[round & 1]);
+        }
         ++round;
         __syncthreads();
-        if (s_best == 0ull && c > 0.0f) {
-            c = 0.0f;
+        if (s_best == 0ull && from_resid) {
+            c_hi = c_lo = 0.0f;
             continue;
         }
         break;
@@ -339,6 +386,8 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
             toks[l0] = a;
             o.bonus[b] = a;
             o.accept_len[b] = l0;
+            if (want_gap) o.margin[b] = fminf(s_margin, s_gap);
+            write_stats(o, b, l0, nn_read, l0 + (a >= 0 ? 1 : 0), s_rej);
         }
         break;
     }
@@ -350,10 +399,11 @@ cudaError_t launch_accept_ratio(const float* logits, const float* draft_logits, 
                                 const int32_t* n_nodes, int B, int N, int D, const float* temperature,
                                 const uint64_t* seed, uint64_t offset, int32_t* accept_len,
                                 int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
-                                int32_t* dev_status, cudaStream_t stream) {
+                                float* margin_stats, int32_t* walk_stats, int32_t* dev_status,
+                                cudaStream_t stream) {
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
                       (reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0);
-    WalkOut o{accept_len, out_tokens, out_nodes, bonus};
+    WalkOut o{accept_len, out_tokens, out_nodes, bonus, margin_stats, walk_stats};
     accept_ratio_kernel<<<B * kCluster, kWalkThreads, 0, stream>>>(
         logits, draft_logits, V, vec4, token, first_child, next_sibling, n_nodes, N, D, temperature, seed,
         offset, o, dev_status);

@@ -7,6 +7,7 @@
 
 #include "attn.cuh"
 #include "common.cuh"
+#include "ddtree_testing.h"
 #include "trace.h"
 
 namespace ddt {
@@ -15,19 +16,31 @@ cudaError_t launch_build(const float*, const int32_t*, const int32_t*, const int
                          int32_t*, int32_t*, uint32_t*, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_accept_greedy(const float*, int, const int32_t*, const int32_t*,
                                  const int32_t*, const int32_t*, int, int, int, int32_t*,
-                                 int32_t*, int32_t*, int32_t*, int32_t*, cudaStream_t);
+                                 int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_accept_sample(const float*, int, const int32_t*, const int32_t*,
                                  const int32_t*, const int32_t*, int, int, int, const float*,
                                  const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*,
-                                 int32_t*, int32_t*, cudaStream_t);
+                                 int32_t*, float*, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_draft_topk(const float*, int, int, int, int, float*, int32_t*, cudaStream_t);
 cudaError_t launch_accept_ratio(const float*, const float*, int, const int32_t*, const int32_t*,
                                 const int32_t*, const int32_t*, int, int, int, const float*,
                                 const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*, int32_t*,
-                                int32_t*, cudaStream_t);
+                                float*, int32_t*, int32_t*, cudaStream_t);
 cudaError_t launch_commit_kv(const ddtree_bf16*, const ddtree_bf16*, const int32_t*, const int32_t*, int,
                              int, int, int, int, ddtree_bf16*, ddtree_bf16*, int, int, const int32_t*,
                              int, const int32_t*, int32_t*, int32_t*, cudaStream_t);
+
+cudaError_t launch_shard_begin(int, int, int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_shard_partial(const float*, int, int, const int32_t*, const int32_t*, const int32_t*,
+                                 const int32_t*, int, int, const float*, const int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_shard_advance(const int32_t*, int, int, int, const int32_t*, const int32_t*, const int32_t*,
+                                 const int32_t*, int, int, const float*, const uint64_t*, uint64_t, int32_t*,
+                                 int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_shard_bonus(const float*, int, int, const int32_t*, const int32_t*, const int32_t*,
+                               const int32_t*, int, int, const float*, const uint64_t*, uint64_t, const int32_t*,
+                               unsigned long long*, cudaStream_t);
+cudaError_t launch_shard_finish(const unsigned long long*, int, int, int, int32_t*, int32_t*, int32_t*, int32_t*,
+                                cudaStream_t);
 
 thread_local char g_last_error[256] = "";
 
@@ -166,14 +179,16 @@ size_t tree_verify_attn_workspace_size(int B, int N, int Hq, int Hkv, int Dh, in
     return pl.ws_o_bytes + pl.ws_ml_bytes;
 }
 
-int tree_verify_attn(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtree_bf16* v_tree,
-                     const ddtree_bf16* k_cache, const ddtree_bf16* v_cache, int num_pages,
-                     int page_size, const int32_t* page_table, int max_pages,
-                     const int32_t* ctx_len, const uint32_t* vis, const int32_t* n_nodes,
-                     int B, int N, int Hq, int Hkv, int Dh, float scale, ddtree_bf16* out,
-                     float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                     void* stream) {
-    TraceRange trace("tree_verify_attn");
+namespace {
+
+// tree_verify_attn's checks and launches; stall_ns != 0 (the testing entry
+// point only) makes the tensor-core kernel's bounded waits run out.
+int attn_call(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtree_bf16* v_tree,
+              const ddtree_bf16* k_cache, const ddtree_bf16* v_cache, int num_pages, int page_size,
+              const int32_t* page_table, int max_pages, const int32_t* ctx_len, const uint32_t* vis,
+              const int32_t* n_nodes, int B, int N, int Hq, int Hkv, int Dh, float scale,
+              ddtree_bf16* out, float* lse, void* workspace, size_t workspace_bytes,
+              int32_t* dev_status, void* stream, uint64_t stall_ns) {
     if (B < 0 || !std::isfinite(scale)) return DDT_EINVAL;
     if (page_size < 16 || page_size > 1024 || page_size % 16 != 0 || num_pages < 1 ||
         max_pages < 1)
@@ -204,15 +219,47 @@ int tree_verify_attn(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtr
     p.R = pl.R; p.rows_per_group = pl.rows_per_group; p.n_groups = pl.n_groups;
     p.tiles_per_chunk = pl.tiles_per_chunk; p.max_chunks = pl.max_chunks;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.stall_ns = stall_ns;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (attn_tc_supported(p)) {
         e = launch_attn_tc(p, st);
         if (e == cudaSuccess) e = launch_attn_combine(p, st);
     } else {
+        if (stall_ns) return DDT_ESHAPE;   // only the tensor-core kernel has bounded waits
         e = launch_attn_mma(p, st);
     }
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+int tree_verify_attn(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtree_bf16* v_tree,
+                     const ddtree_bf16* k_cache, const ddtree_bf16* v_cache, int num_pages,
+                     int page_size, const int32_t* page_table, int max_pages,
+                     const int32_t* ctx_len, const uint32_t* vis, const int32_t* n_nodes,
+                     int B, int N, int Hq, int Hkv, int Dh, float scale, ddtree_bf16* out,
+                     float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream) {
+    TraceRange trace("tree_verify_attn");
+    return attn_call(q, k_tree, v_tree, k_cache, v_cache, num_pages, page_size, page_table, max_pages,
+                     ctx_len, vis, n_nodes, B, N, Hq, Hkv, Dh, scale, out, lse, workspace,
+                     workspace_bytes, dev_status, stream, 0);
+}
+
+int ddtree_testing_attn_stall(const ddtree_bf16* q, const ddtree_bf16* k_tree,
+                              const ddtree_bf16* v_tree, const ddtree_bf16* k_cache,
+                              const ddtree_bf16* v_cache, int num_pages, int page_size,
+                              const int32_t* page_table, int max_pages, const int32_t* ctx_len,
+                              const uint32_t* vis, const int32_t* n_nodes, int B, int N, int Hq,
+                              int Hkv, int Dh, float scale, ddtree_bf16* out, float* lse,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                              void* stream, uint64_t stall_ns) {
+    TraceRange trace("ddtree_testing_attn_stall");
+    if (stall_ns == 0 || stall_ns > 1000000000ull) return DDT_EINVAL;
+    return attn_call(q, k_tree, v_tree, k_cache, v_cache, num_pages, page_size, page_table, max_pages,
+                     ctx_len, vis, n_nodes, B, N, Hq, Hkv, Dh, scale, out, lse, workspace,
+                     workspace_bytes, dev_status, stream, stall_ns);
 }
 
 static int check_walk_args(const float* logits, int V, const int32_t* token,
@@ -232,13 +279,13 @@ int ddtree_accept_greedy(const float* logits, int V, const int32_t* token,
                          const int32_t* first_child, const int32_t* next_sibling,
                          const int32_t* n_nodes, int B, int N, int D, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
-                         int32_t* dev_status, void* stream) {
+                         int32_t* walk_stats, int32_t* dev_status, void* stream) {
     TraceRange trace("ddtree_accept_greedy");
     int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
                              accept_len, out_tokens, out_nodes, bonus);
     if (st != DDT_OK || B == 0) return st;
     cudaError_t e = launch_accept_greedy(logits, V, token, first_child, next_sibling, n_nodes, B,
-                                         N, D, accept_len, out_tokens, out_nodes, bonus,
+                                         N, D, accept_len, out_tokens, out_nodes, bonus, walk_stats,
                                          dev_status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
@@ -248,7 +295,8 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                          const int32_t* n_nodes, int B, int N, int D, const float* temperature,
                          const uint64_t* seed, uint64_t philox_offset, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
-                         int32_t* dev_status, void* stream) {
+                         float* margin_stats, int32_t* walk_stats, int32_t* dev_status,
+                         void* stream) {
     TraceRange trace("ddtree_accept_sample");
     int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
                              accept_len, out_tokens, out_nodes, bonus);
@@ -257,8 +305,8 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
     if (philox_offset >> 56) return DDT_EINVAL;
     cudaError_t e = launch_accept_sample(logits, V, token, first_child, next_sibling, n_nodes, B,
                                          N, D, temperature, seed, philox_offset, accept_len,
-                                         out_tokens, out_nodes, bonus, dev_status,
-                                         static_cast<cudaStream_t>(stream));
+                                         out_tokens, out_nodes, bonus, margin_stats, walk_stats,
+                                         dev_status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
 
@@ -267,8 +315,8 @@ int ddtree_accept_sample_ratio(const float* logits, const float* draft_logits, i
                                const int32_t* next_sibling, const int32_t* n_nodes, int B, int N,
                                int D, const float* temperature, const uint64_t* seed,
                                uint64_t philox_offset, int32_t* accept_len, int32_t* out_tokens,
-                               int32_t* out_nodes, int32_t* bonus, int32_t* dev_status,
-                               void* stream) {
+                               int32_t* out_nodes, int32_t* bonus, float* margin_stats,
+                               int32_t* walk_stats, int32_t* dev_status, void* stream) {
     TraceRange trace("ddtree_accept_sample_ratio");
     int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
                              accept_len, out_tokens, out_nodes, bonus);
@@ -277,8 +325,8 @@ int ddtree_accept_sample_ratio(const float* logits, const float* draft_logits, i
     if (philox_offset >> 56) return DDT_EINVAL;
     cudaError_t e = launch_accept_ratio(logits, draft_logits, V, token, first_child, next_sibling,
                                         n_nodes, B, N, D, temperature, seed, philox_offset,
-                                        accept_len, out_tokens, out_nodes, bonus, dev_status,
-                                        static_cast<cudaStream_t>(stream));
+                                        accept_len, out_tokens, out_nodes, bonus, margin_stats,
+                                        walk_stats, dev_status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
 
@@ -302,6 +350,94 @@ int ddtree_commit_kv(const ddtree_bf16* k_tree, const ddtree_bf16* v_tree, const
     cudaError_t e = launch_commit_kv(k_tree, v_tree, out_nodes, accept_len, B, N, D, Hkv, Dh, k_cache,
                                      v_cache, num_pages, page_size, page_table, max_pages, ctx_len,
                                      new_ctx_len, dev_status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------------------
+// the walks over a vocabulary-parallel logits shard (requests split over GPUs by KV head)
+// ---------------------------------------------------------------------------
+
+static int check_shard_tree(const int32_t* token, const int32_t* first_child, const int32_t* next_sibling,
+                            const int32_t* n_nodes, int B, int N) {
+    if (B < 0) return DDT_EINVAL;
+    if (N < 1 || N > DDT_MAX_NODES) return DDT_ESHAPE;
+    if (B > 0 && (!token || !first_child || !next_sibling || !n_nodes)) return DDT_EINVAL;
+    return DDT_OK;
+}
+
+int ddtree_shard_walk_begin(int B, int D, int32_t* state, int32_t* accept_len, int32_t* out_tokens,
+                            int32_t* out_nodes, int32_t* bonus, void* stream) {
+    TraceRange trace("ddtree_shard_walk_begin");
+    if (B < 0) return DDT_EINVAL;
+    if (D < 1 || D > DDT_MAX_DEPTH) return DDT_ESHAPE;
+    if (B == 0) return DDT_OK;
+    if (!state || !accept_len || !out_tokens || !out_nodes || !bonus) return DDT_EINVAL;
+    cudaError_t e = launch_shard_begin(B, D, state, accept_len, out_tokens, out_nodes, bonus,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+int ddtree_shard_walk_partial(const float* logits_shard, int Vs, int v0, int V, const int32_t* token,
+                              const int32_t* first_child, const int32_t* next_sibling,
+                              const int32_t* n_nodes, int B, int N, const float* temperature,
+                              const int32_t* state, int32_t* record, void* stream) {
+    TraceRange trace("ddtree_shard_walk_partial");
+    int st = check_shard_tree(token, first_child, next_sibling, n_nodes, B, N);
+    if (st != DDT_OK) return st;
+    if (Vs < 1 || v0 < 0 || V < 1 || static_cast<long long>(v0) + Vs > V) return DDT_EINVAL;
+    if (B == 0) return DDT_OK;
+    if (!logits_shard || !state || !record) return DDT_EINVAL;
+    cudaError_t e = launch_shard_partial(logits_shard, Vs, v0, token, first_child, next_sibling, n_nodes, B, N,
+                                         temperature, state, record, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+int ddtree_shard_walk_advance(const int32_t* records, int world, int V, const int32_t* token,
+                              const int32_t* first_child, const int32_t* next_sibling,
+                              const int32_t* n_nodes, int B, int N, int D, const float* temperature,
+                              const uint64_t* seed, uint64_t philox_offset, int32_t* state,
+                              int32_t* accept_len, int32_t* out_tokens, int32_t* out_nodes, int32_t* bonus,
+                              int32_t* dev_status, void* stream) {
+    TraceRange trace("ddtree_shard_walk_advance");
+    int st = check_shard_tree(token, first_child, next_sibling, n_nodes, B, N);
+    if (st != DDT_OK) return st;
+    if (world < 1 || world > 1024 || V < 1) return DDT_EINVAL;
+    if (D < 1 || D > DDT_MAX_DEPTH) return DDT_ESHAPE;
+    if (B == 0) return DDT_OK;
+    if (!records || !state || !accept_len || !out_tokens || !out_nodes || !bonus) return DDT_EINVAL;
+    if (temperature && (!seed || (philox_offset >> 56))) return DDT_EINVAL;
+    cudaError_t e = launch_shard_advance(records, world, B, V, token, first_child, next_sibling, n_nodes, N, D,
+                                         temperature, seed, philox_offset, state, accept_len, out_tokens,
+                                         out_nodes, bonus, dev_status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+int ddtree_shard_walk_bonus(const float* logits_shard, int Vs, int v0, int V, const int32_t* token,
+                            const int32_t* first_child, const int32_t* next_sibling, const int32_t* n_nodes,
+                            int B, int N, const float* temperature, const uint64_t* seed,
+                            uint64_t philox_offset, const int32_t* state, int64_t* key, void* stream) {
+    TraceRange trace("ddtree_shard_walk_bonus");
+    int st = check_shard_tree(token, first_child, next_sibling, n_nodes, B, N);
+    if (st != DDT_OK) return st;
+    if (Vs < 1 || v0 < 0 || V < 1 || static_cast<long long>(v0) + Vs > V) return DDT_EINVAL;
+    if (B == 0) return DDT_OK;
+    if (!logits_shard || !temperature || !seed || !state || !key || (philox_offset >> 56)) return DDT_EINVAL;
+    cudaError_t e = launch_shard_bonus(logits_shard, Vs, v0, token, first_child, next_sibling, n_nodes, B, N,
+                                       temperature, seed, philox_offset, state,
+                                       reinterpret_cast<unsigned long long*>(key),
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+int ddtree_shard_walk_finish(const int64_t* keys, int world, int B, int D, int32_t* state,
+                             int32_t* accept_len, int32_t* out_tokens, int32_t* bonus, void* stream) {
+    TraceRange trace("ddtree_shard_walk_finish");
+    if (B < 0 || world < 1 || world > 1024) return DDT_EINVAL;
+    if (D < 1 || D > DDT_MAX_DEPTH) return DDT_ESHAPE;
+    if (B == 0) return DDT_OK;
+    if (!keys || !state || !accept_len || !out_tokens || !bonus) return DDT_EINVAL;
+    cudaError_t e = launch_shard_finish(reinterpret_cast<const unsigned long long*>(keys), world, B, D, state,
+                                        accept_len, out_tokens, bonus, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
 

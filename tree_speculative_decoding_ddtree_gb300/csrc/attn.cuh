@@ -29,6 +29,7 @@ struct AttnParams {
     int rows_per_group, n_groups;
     int tiles_per_chunk, max_chunks;
     float scale_log2;
+    uint64_t stall_ns;   // 0; else (testing entry point only) a wait that nothing completes, bounded by this limit
 };
 
 // warp-MMA path: any supported shape (split-KV main launch + combine)

@@ -87,6 +87,7 @@ struct TcShared {
     uint64_t p_full[2];       // [tile]: P written over it
     uint64_t o_final;
     uint64_t vfix[3];
+    uint64_t never;           // completed by nothing: the testing entry point's stalled wait
     uint32_t tmem_base;
     int abort;
     float side_max[2][4][kMaxSide];
@@ -283,6 +284,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         }
         mbar_init(bar_addr(sh.o_final), 1);
         for (int k = 0; k < 3; ++k) mbar_init(bar_addr(sh.vfix[k]), 1);
+        mbar_init(bar_addr(sh.never), 1);
         sh.abort = 0;
         fence_mbar_init();
     }
@@ -430,7 +432,12 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             auto wait_all = [&](uint32_t bar, uint32_t parity) {
                 return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort));
             };
-            bool ok = wait_all(bar_addr(sh.q_tmem), 0) && (g.n_tiles == 0 || wait_all(bar_addr(sh.kv_full[0]), 0));
+            // testing entry point only: a wait that nothing completes runs out after
+            // stall_ns and aborts the CTA through the normal path
+            const bool stalled = p.stall_ns != 0 &&
+                                 !__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.never), 0, abort, p.stall_ns));
+            bool ok = !stalled && wait_all(bar_addr(sh.q_tmem), 0) &&
+                      (g.n_tiles == 0 || wait_all(bar_addr(sh.kv_full[0]), 0));
             if (ok && g.n_tiles > 0) {
                 tc_fence_after();
                 qk(0, 0);

@@ -35,16 +35,16 @@ int record_step(const ddtree_step_args& a, cudaStream_t s) {
     if (a.walk == 0)
         st = ddtree_accept_greedy(a.logits, a.V, a.token, a.first_child, a.next_sibling, a.n_nodes,
                                   a.B, N, a.D, a.accept_len, a.out_tokens, a.out_nodes, a.bonus,
-                                  a.dev_status, s);
+                                  nullptr, a.dev_status, s);
     else if (a.walk == 1)
         st = ddtree_accept_sample(a.logits, a.V, a.token, a.first_child, a.next_sibling, a.n_nodes,
                                   a.B, N, a.D, a.temperature, a.seed, a.philox_offset, a.accept_len,
-                                  a.out_tokens, a.out_nodes, a.bonus, a.dev_status, s);
+                                  a.out_tokens, a.out_nodes, a.bonus, nullptr, nullptr, a.dev_status, s);
     else
         st = ddtree_accept_sample_ratio(a.logits, a.draft_logits, a.V, a.token, a.first_child,
                                         a.next_sibling, a.n_nodes, a.B, N, a.D, a.temperature, a.seed,
                                         a.philox_offset, a.accept_len, a.out_tokens, a.out_nodes,
-                                        a.bonus, a.dev_status, s);
+                                        a.bonus, nullptr, nullptr, a.dev_status, s);
     if (st != DDT_OK) return st;
     return ddtree_commit_kv(a.k_tree, a.v_tree, a.out_nodes, a.accept_len, a.B, N, a.D, a.Hkv, a.Dh,
                             a.k_cache, a.v_cache, a.num_pages, a.page_size, a.page_table,

@@ -37,9 +37,9 @@ DDT_DEVINL unsigned long long ld_cluster_u64(uint32_t addr) {
     asm volatile("ld.shared::cluster.u64 %0, [%1];\n" : "=l"(v) : "r"(addr) : "memory");
     return v;
 }
-DDT_DEVINL float ld_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
+DDT_DEVINL double ld_cluster_f64(uint32_t addr) {
+    double v;
+    asm volatile("ld.shared::cluster.f64 %0, [%1];\n" : "=d"(v) : "r"(addr) : "memory");
     return v;
 }
 DDT_DEVINL float2 ld_cluster_f32x2(uint32_t addr) {
@@ -156,7 +156,65 @@ struct WalkOut {
     int32_t* out_tokens;
     int32_t* out_nodes;
     int32_t* bonus;
+    float* margin;        // nullable [B]: smallest decision margin on the path
+    int32_t* stats;       // nullable [B, 4]: accepted depth, nodes built, tokens emitted,
+                          //                  child tests that rejected (or did not match)
 };
+
+// Write one request's walk statistics (writer CTA, one thread).
+DDT_DEVINL void write_stats(const WalkOut& o, int b, int len, int n_nodes, int emitted, int rejected) {
+    if (!o.stats) return;
+    int32_t* st = o.stats + static_cast<size_t>(b) * 4;
+    st[0] = len;
+    st[1] = n_nodes;
+    st[2] = emitted;
+    st[3] = rejected;
+}
+
+// ---------------------------------------------------------------------------
+// The bonus draw's decision margin: the gap between the best and the
+// runner-up perturbed score. Each thread keeps the two largest scores it saw
+// (only when a caller asked for margins); pairs merge by (max of the tops,
+// max of the smaller top and the runner-ups).
+// ---------------------------------------------------------------------------
+struct Gap2 {
+    float top, sec;
+};
+DDT_DEVINL void gap2_add(Gap2& g, float sc) {
+    g.sec = fmaxf(g.sec, fminf(g.top, sc));
+    g.top = fmaxf(g.top, sc);
+}
+DDT_DEVINL Gap2 gap2_merge(Gap2 x, Gap2 y) {
+    return Gap2{fmaxf(x.top, y.top), fmaxf(fminf(x.top, y.top), fmaxf(x.sec, y.sec))};
+}
+// block-wide merge over kWalkThreads threads; thread 0 gets the result
+DDT_DEVINL Gap2 block_gap2(Gap2 g, float2* scratch /* [32] */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        g = gap2_merge(g, Gap2{__shfl_xor_sync(0xffffffffu, g.top, o), __shfl_xor_sync(0xffffffffu, g.sec, o)});
+    __syncthreads();
+    if (lane == 0) scratch[warp] = make_float2(g.top, g.sec);
+    __syncthreads();
+    if (warp == 0) {
+        const float2 v = lane < kWalkThreads / 32 ? scratch[lane] : make_float2(-INFINITY, -INFINITY);
+        g = Gap2{v.x, v.y};
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            g = gap2_merge(g, Gap2{__shfl_xor_sync(0xffffffffu, g.top, o), __shfl_xor_sync(0xffffffffu, g.sec, o)});
+    }
+    return g;
+}
+// merge of the cluster's partials (float2 `part` in every CTA, rank order): the gap
+DDT_DEVINL float cluster_gap(const float2* part) {
+    Gap2 g{-INFINITY, -INFINITY};
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) {
+        const float2 v = ld_cluster_f32x2(cluster_addr(part, r));
+        g = gap2_merge(g, Gap2{v.x, v.y});
+    }
+    return g.sec == -INFINITY ? INFINITY : g.top - g.sec;
+}
 
 // The request's token / first-child / next-sibling rows, staged in shared
 // memory so the serial child scans never wait on global memory.
@@ -187,5 +245,6 @@ DDT_DEVINL MaxSum merge_ms(MaxSum a, MaxSum b, float inv_t) {
     r.z = (M == -INFINITY) ? 0.0f : a.z * expf((a.m - M) * inv_t) + b.z * expf((b.m - M) * inv_t);
     return r;
 }
+
 
 }  // namespace ddt
