@@ -93,5 +93,9 @@ def test_reference_line_carries_the_contract_keys():
     w = S.config("tiny")
     assert line["config"]["workload"] == "tiny" and line["config"]["global_batch"] == w.B
     assert line["config"]["seq_len"] == bench.mean_context(w) == 256   # the tiny workload's fixed context
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == (os.cpu_count() or 1) and cb["nproc"] == os.cpu_count()
+    assert cb["cpu_model"]
     assert line["e2e"]["value"] == line["value"]
+    # every reported step is a full oracle step that ran inside the command
+    assert line["ms_per_step"] * (line["steps"] + line["warmup"]) / 1e3 <= line["wall_s"]
