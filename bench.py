@@ -41,13 +41,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tree-verify steps/s & attn HBM GB/s (% roofline), batch16 ctx8k budget32"
 # DRAM traffic of one attn_tc_kernel launch on the batched workload:
-# dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture (--set full,
-# one launch) of `bench.py --steps 5 --warmup 3 --no-cpu-baseline --e2e-steps 3`.
-# The kernel has changed since that capture (the O rescale is now decided per
-# warp; its memory accesses are unchanged), so the reported traffic is None
-# until the next capture and the captured figure is given beside it.
-ATTN_TC_TRAFFIC_BYTES = None
-ATTN_TC_TRAFFIC_LAST_CAPTURE = 533.647360e6 + 25.676544e6
+# dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture (a metric
+# list, one launch) of `bench.py --steps 5 --warmup 3 --no-cpu-baseline
+# --e2e-steps 3`, on the current kernel (profiles/attn_tc_batched16_ctx8k.md).
+ATTN_TC_TRAFFIC_BYTES = 533646848 + 25419264
 WORKLOAD_DESC = ("batched serving: 16 requests, ctx ~U[1024,16384] paged (page 64, shuffled), "
                  "Hq 64 / Hkv 8 / Dh 128 bf16, budget 32 (N=33), top-k 8, depth 8, vocab 32000")
 
@@ -710,9 +707,6 @@ def run_native(args):
                          "frac": achieved / hbm_peak,
                          "traffic": ATTN_TC_TRAFFIC_BYTES if w.name == "batched" else None,
                          "traffic_source": "ncu dram read+write of one attn_tc_kernel launch, batched workload",
-                         "traffic_last_capture": (ATTN_TC_TRAFFIC_LAST_CAPTURE if w.name == "batched" else None),
-                         "traffic_note": ("null: the kernel changed after the capture (per-warp rescale "
-                                          "decision, same memory accesses); last capture given beside it"),
                          "kernel": "tree_verify_attn (split-KV main + combine launches)",
                          "peak_source": f"{peak_src} hbm_gbs",
                          "algorithmic_bytes": abytes, "attn_us": attn_avg_ms * 1e3,
