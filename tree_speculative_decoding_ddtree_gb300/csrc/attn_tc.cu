@@ -63,7 +63,7 @@ constexpr uint32_t kStageBytes = 4 * kHalfBytes;        // K0 K1 V0 V1
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffStages = 2 * kQTileBytes;                       // 64 KB
 constexpr uint32_t kOffSideO = kOffStages + kStages * kStageBytes;     // 192 KB
-constexpr uint32_t kSideOBytes = kD * kMaxSide * 4;                    // 4 KB
+constexpr uint32_t kSideOBytes = 4 * kMaxSide * kD * 4;                // 16 KB: one block per leftover-row warp
 constexpr uint32_t kSmemBytes = kOffSideO + kSideOBytes + 1024;        // + alignment slack
 
 constexpr uint32_t kColS = 0;     // + 64 * t: S of tile t, P written over its first 32 columns
@@ -85,7 +85,7 @@ struct TcShared {
     uint64_t q_tmem;          // Q rows copied from shared memory into TMEM
     uint64_t s_full[2];       // [tile]: S of the current key tile is in TMEM
     uint64_t p_full[2];       // [tile]: P written over it
-    uint64_t o_final;
+    uint64_t o_final[2];      // row tile t's last PV done: its epilogue may read O
     uint64_t vfix[3];
     uint64_t never;           // completed by nothing: the testing entry point's stalled wait
     uint32_t tmem_base;
@@ -217,12 +217,52 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+    // ---------------- set-up: barriers, descriptors, TMEM ----------------
+    // None of it depends on the work item (every CTA has the same rows), so it
+    // runs beside the item lookup, under one barrier.
+    {
+        const int n_main = p.R > 128 ? 2 : 1;
+        const bool side = p.R > 256;
+        if (tid == 64) {   // warp 2: idle during the lookup
+            mbar_init(bar_addr(sh.q_full), 1);
+            for (int s = 0; s < kStages; ++s) {
+                mbar_init(bar_addr(sh.kv_full[s]), 1);
+                mbar_init(bar_addr(sh.kv_empty[s]), side ? 5 : 1);   // MMA commit + 4 side warps
+            }
+            mbar_init(bar_addr(sh.q_tmem), 4 * n_main);   // one arrival per softmax warp
+            for (int t = 0; t < 2; ++t) {
+                mbar_init(bar_addr(sh.s_full[t]), 1);
+                mbar_init(bar_addr(sh.p_full[t]), 4);
+            }
+            mbar_init(bar_addr(sh.o_final[0]), 1);
+            mbar_init(bar_addr(sh.o_final[1]), 1);
+            for (int k = 0; k < 3; ++k) mbar_init(bar_addr(sh.vfix[k]), 1);
+            mbar_init(bar_addr(sh.never), 1);
+            sh.abort = 0;
+            fence_mbar_init();
+            prefetch_tmap(&maps.q);
+            prefetch_tmap(&maps.kc);
+            prefetch_tmap(&maps.vc);
+            prefetch_tmap(&maps.kt);
+            prefetch_tmap(&maps.vt);
+        }
+        if (warp == 1) tmem_alloc(smem_u32(&sh.tmem_base), 512);
+    }
+    const bool lpt = p.B <= kLptMaxB && p.max_chunks > 1;
+    if (lpt && warp == 0) lpt_item(p, static_cast<int>(blockIdx.x), sh.map_cnt, sh.map_off, sh.item);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = sh.tmem_base;
+    // a CTA without work frees its TMEM and leaves (nothing is in flight yet)
+    auto leave = [&]() {
+        if (warp == 1) tmem_dealloc(tbase, 512);
+    };
+
     Geometry g;
     int nn_loaded;
-    if (p.B <= kLptMaxB && p.max_chunks > 1) {   // one-dimensional grid, longest chunks first
-        if (warp == 0) lpt_item(p, static_cast<int>(blockIdx.x), sh.map_cnt, sh.map_off, sh.item);
-        __syncthreads();
-        if (!sh.item[3]) return;
+    if (lpt) {   // one-dimensional grid, longest chunks first
+        if (!sh.item[3]) { leave(); return; }
         g.b = sh.item[0];
         g.kvh = sh.item[1];
         g.chunk = sh.item[2];
@@ -242,7 +282,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     if (g.L < 0 || g.L > p.max_pages * p.page_size) { g.bad = true; g.L = 0; }
     const int nt_ctx = (g.L + kKeys - 1) / kKeys;
     g.nchunks = nt_ctx > 0 ? (nt_ctx + p.tiles_per_chunk - 1) / p.tiles_per_chunk : 1;
-    if (g.chunk >= g.nchunks) return;
+    if (g.chunk >= g.nchunks) { leave(); return; }
     g.nn = nn_loaded;
     if (g.nn < 0 || g.nn > p.N) { g.bad = true; g.nn = 0; }
     // the request's tiles in nchunks chunks of equal length (within one tile)
@@ -264,35 +304,13 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                 if (p.lse && c == 0) p.lse[(static_cast<size_t>(g.b) * p.N + i) * p.Hq + h] = -INFINITY;
             }
         }
+        leave();
         return;
     }
 
     const size_t slot = (static_cast<size_t>(g.b) * p.Hkv + g.kvh) * p.max_chunks + g.chunk;
     const bool split = g.nchunks > 1;
 
-    // ---------------- set-up: barriers and TMEM ----------------
-    if (tid == 0) {
-        mbar_init(bar_addr(sh.q_full), 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_addr(sh.kv_full[s]), 1);
-            mbar_init(bar_addr(sh.kv_empty[s]), g.n_side > 0 ? 5 : 1);   // MMA commit + 4 side warps
-        }
-        mbar_init(bar_addr(sh.q_tmem), 4 * g.n_main);   // one arrival per softmax warp
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(bar_addr(sh.s_full[t]), 1);
-            mbar_init(bar_addr(sh.p_full[t]), 4);
-        }
-        mbar_init(bar_addr(sh.o_final), 1);
-        for (int k = 0; k < 3; ++k) mbar_init(bar_addr(sh.vfix[k]), 1);
-        mbar_init(bar_addr(sh.never), 1);
-        sh.abort = 0;
-        fence_mbar_init();
-    }
-    if (warp == 1) tmem_alloc(smem_u32(&sh.tmem_base), 512);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = sh.tmem_base;
     volatile int* abort = &sh.abort;
 
     const uint32_t sQ = smem_u32(smem + kOffQ);
@@ -306,11 +324,6 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
         int pf_base = -1, pf_page = 0;
         if (lane == 0) {
-            prefetch_tmap(&maps.q);
-            prefetch_tmap(&maps.kc);
-            prefetch_tmap(&maps.vc);
-            prefetch_tmap(&maps.kt);
-            prefetch_tmap(&maps.vt);
             mbar_arrive_expect_tx(bar_addr(sh.q_full), g.n_main * kQTileBytes);
             const int nodes_per_tile = 128 / g.G;
             for (int t = 0; t < g.n_main; ++t)
@@ -436,6 +449,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             // stall_ns and aborts the CTA through the normal path
             const bool stalled = p.stall_ns != 0 &&
                                  !__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.never), 0, abort, p.stall_ns));
+            bool fin[2] = {false, false};   // o_final[t] committed
             bool ok = !stalled && wait_all(bar_addr(sh.q_tmem), 0) &&
                       (g.n_tiles == 0 || wait_all(bar_addr(sh.kv_full[0]), 0));
             if (ok && g.n_tiles > 0) {
@@ -450,6 +464,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                 if (!wait_all(bar_addr(sh.p_full[0]), j & 1)) break;
                 tc_fence_after();
                 pv(0, j);
+                if (!more) { mma_commit_elect(bar_addr(sh.o_final[0])); fin[0] = true; }
                 if (more) {
                     if (!wait_all(bar_addr(sh.kv_full[(j + 1) % kStages]), ((j + 1) / kStages) & 1)) break;
                     tc_fence_after();
@@ -459,12 +474,16 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                     if (!wait_all(bar_addr(sh.p_full[1]), j & 1)) break;
                     tc_fence_after();
                     pv(1, j);
+                    if (!more) { mma_commit_elect(bar_addr(sh.o_final[1])); fin[1] = true; }
                 }
                 mma_commit_elect(bar_addr(sh.kv_empty[j % kStages]));   // K_j and V_j consumed
                 if (g.n_main == 2 && more) qk(1, j + 1);
             }
-            mma_commit_elect(bar_addr(sh.o_final));
-            mbar_drain(bar_addr(sh.o_final), 0);   // every MMA done before TMEM is freed
+            // a tile whose last PV was not reached (abort, or no tiles) is released here
+            for (int t = 0; t < g.n_main; ++t)
+                if (!fin[t]) mma_commit_elect(bar_addr(sh.o_final[t]));
+            for (int t = 0; t < g.n_main; ++t)
+                mbar_drain(bar_addr(sh.o_final[t]), 0);   // every MMA done before TMEM is freed
         }
         __syncwarp();
     } else if (warp >= 4 && warp < 12) {
@@ -596,7 +615,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             if (lane == 0) mbar_arrive(bar_addr(sh.p_full[t]));   // one arrival per warp
         }
         if (active) {
-            const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.o_final), 0, abort));
+            const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.o_final[t]), 0, abort));
             tc_fence_after();
             const int i = node, h = g.kvh * g.G + (valid_row ? r % g.G : 0);
             const bool good = done && ok;
@@ -782,8 +801,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             l_part[q] += __shfl_xor_sync(0xffffffffu, l_part[q], 8);
             l_part[q] += __shfl_xor_sync(0xffffffffu, l_part[q], 16);
         }
-        float* side_o = reinterpret_cast<float*>(smem + kOffSideO);   // [kD][kMaxSide]
-        for (int x = tid - 384; x < kD * kMaxSide; x += 128) side_o[x] = 0.0f;
+        // [4 warps][kMaxSide rows][kD]: each warp writes every entry of its own block
+        float* side_o = reinterpret_cast<float*>(smem + kOffSideO);
         if (lane < 4) {
             sh.side_max[0][sw][crow0] = m_run[0];
             sh.side_max[0][sw][crow0 + 1] = m_run[1];
@@ -802,18 +821,37 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             sh.side_l[sw][crow0] = l_part[0] * wscale[0];
             sh.side_l[sw][crow0 + 1] = l_part[1] * wscale[1];
         }
+        {
+            float* mine = side_o + sw * (kMaxSide * kD);
 #pragma unroll
-        for (int mb = 0; mb < kD / 16; ++mb) {
-            const int d0 = 16 * mb + nrow;
-            atomicAdd(&side_o[d0 * kMaxSide + crow0], oacc[mb][0] * wscale[0]);
-            atomicAdd(&side_o[d0 * kMaxSide + crow0 + 1], oacc[mb][1] * wscale[1]);
-            atomicAdd(&side_o[(d0 + 8) * kMaxSide + crow0], oacc[mb][2] * wscale[0]);
-            atomicAdd(&side_o[(d0 + 8) * kMaxSide + crow0 + 1], oacc[mb][3] * wscale[1]);
+            for (int mb = 0; mb < kD / 16; ++mb) {
+                const int d0 = 16 * mb + nrow;
+                mine[crow0 * kD + d0] = oacc[mb][0] * wscale[0];
+                mine[(crow0 + 1) * kD + d0] = oacc[mb][1] * wscale[1];
+                mine[crow0 * kD + d0 + 8] = oacc[mb][2] * wscale[0];
+                mine[(crow0 + 1) * kD + d0 + 8] = oacc[mb][3] * wscale[1];
+            }
         }
         named_bar_sync(1, 128);
-        // write: thread -> (row tid/16, 8 features)
+        // write: thread -> (row tid/16, 8 features), the four warps' blocks summed in
+        // a fixed order
         const int st = tid - 384;
         const int sr = st >> 4, d0 = (st & 15) * 8;
+        float o8[8];
+        {
+            const float* src = side_o + sr * kD + d0;
+            const float4 a0 = *reinterpret_cast<const float4*>(src);
+            const float4 a1 = *reinterpret_cast<const float4*>(src + 4);
+            o8[0] = a0.x; o8[1] = a0.y; o8[2] = a0.z; o8[3] = a0.w;
+            o8[4] = a1.x; o8[5] = a1.y; o8[6] = a1.z; o8[7] = a1.w;
+#pragma unroll
+            for (int w2 = 1; w2 < 4; ++w2) {
+                const float4 b0 = *reinterpret_cast<const float4*>(src + w2 * (kMaxSide * kD));
+                const float4 b1 = *reinterpret_cast<const float4*>(src + w2 * (kMaxSide * kD) + 4);
+                o8[0] += b0.x; o8[1] += b0.y; o8[2] += b0.z; o8[3] += b0.w;
+                o8[4] += b1.x; o8[5] += b1.y; o8[6] += b1.z; o8[7] += b1.w;
+            }
+        }
         if (sr < g.n_side) {
             const int r = 256 + sr;
             const int i = r / g.G, h = g.kvh * g.G + r % g.G;
@@ -825,8 +863,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    __nv_bfloat162 v = __floats2bfloat162_rn(inv != 0.0f ? side_o[(d0 + 2 * e) * kMaxSide + sr] * inv : 0.0f,
-                                                             inv != 0.0f ? side_o[(d0 + 2 * e + 1) * kMaxSide + sr] * inv : 0.0f);
+                    __nv_bfloat162 v = __floats2bfloat162_rn(inv != 0.0f ? o8[2 * e] * inv : 0.0f,
+                                                             inv != 0.0f ? o8[2 * e + 1] * inv : 0.0f);
                     w[e] = *reinterpret_cast<uint32_t*>(&v);
                 }
                 *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD + d0) =
@@ -836,8 +874,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                         (real && lt > 0.0f) ? (mrun + log2f(lt)) * 0.69314718055994531f : -INFINITY;
             } else {
                 float* dst = p.ws_o + (slot * p.R + r) * kD + d0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) dst[e] = ok ? side_o[(d0 + e) * kMaxSide + sr] : 0.0f;
+                *reinterpret_cast<float4*>(dst) = ok ? make_float4(o8[0], o8[1], o8[2], o8[3]) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                *reinterpret_cast<float4*>(dst + 4) = ok ? make_float4(o8[4], o8[5], o8[6], o8[7]) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 if (d0 == 0) p.ws_ml[slot * p.R + r] = ok ? make_float2(mrun, lt) : make_float2(-INFINITY, 0.0f);
             }
         }
