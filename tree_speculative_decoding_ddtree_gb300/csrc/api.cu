@@ -218,6 +218,8 @@ int attn_call(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtree_bf16
     p.B = B; p.N = N; p.Hq = Hq; p.Hkv = Hkv; p.Dh = Dh; p.G = Hq / Hkv; p.W = (N + 31) / 32;
     p.R = pl.R; p.rows_per_group = pl.rows_per_group; p.n_groups = pl.n_groups;
     p.tiles_per_chunk = pl.tiles_per_chunk; p.max_chunks = pl.max_chunks;
+    // fewer merge rows than 32 warps per SM: occupancy cannot hide the loads
+    p.merge_wide = static_cast<long long>(pl.R) * Hkv * B <= 32ll * plan_sms() ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.stall_ns = stall_ns;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -28,6 +28,7 @@ struct AttnParams {
     int B, N, Hq, Hkv, Dh, G, W, R;
     int rows_per_group, n_groups;
     int tiles_per_chunk, max_chunks;
+    int merge_wide;      // split-KV merge with several chunk loads in flight per warp (few rows per SM)
     float scale_log2;
     uint64_t stall_ns;   // 0; else (testing entry point only) a wait that nothing completes, bounded by this limit
 };

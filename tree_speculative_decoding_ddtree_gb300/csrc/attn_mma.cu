@@ -18,6 +18,8 @@
 // ancestor bitmask. Chunks of a multi-chunk request write unnormalised fp32
 // partials that a second launch merges.
 #include "common.cuh"
+#include <type_traits>
+
 #include "attn.cuh"
 
 namespace ddt {
@@ -372,6 +374,105 @@ attn_combine_kernel(AttnParams p) {
             (real && lsum > 0.0f) ? (M + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
 }
 
+// The same merge for launches with few rows per SM (a small batch split into
+// many chunks), where occupancy cannot hide the load latency: the chunks'
+// vectors are loaded kMergeBatch at a time, all issued before any of them is
+// used and before the common max is known (they do not depend on it); the
+// lanes read the chunks' (max, sum) pairs in parallel for the common max and
+// the total, and the weights exp2(max_c - M) reach every lane by shuffles.
+// Same arithmetic in the same order as attn_combine_kernel.
+constexpr int kMergeBatch = 8;
+static_assert(32 % kMergeBatch == 0, "a batch of chunks stays within one lane word of weights");
+template <int DH>
+__global__ void __launch_bounds__(256)
+attn_combine_wide_kernel(AttnParams p) {
+    const int b = blockIdx.z, kvh = blockIdx.y;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= p.R) return;
+    int L = p.ctx_len[b];
+    if (L < 0 || L > p.max_pages * p.page_size) return;
+    const int nt_ctx = (L + kKeyTile - 1) / kKeyTile;
+    const int nchunks = nt_ctx > 0 ? (nt_ctx + p.tiles_per_chunk - 1) / p.tiles_per_chunk : 1;
+    if (nchunks == 1) return;
+    int nn = p.n_nodes[b];
+    const bool nn_ok = nn >= 0 && nn <= p.N;
+    const int G = p.G;
+    const int i = r / G, h = kvh * G + r % G;
+    constexpr int PER = DH / 32;
+    using VecT = typename std::conditional<PER == 4, float4, float2>::type;
+    bf16_t* dst = p.out + ((static_cast<size_t>(b) * p.N + i) * p.Hq + h) * DH + lane * PER;
+    if (!nn_ok) {
+        // A malformed tree: the main kernel flagged it and may have left this
+        // request's partials unwritten, so they are not read. Zeros, lse -inf.
+#pragma unroll
+        for (int e = 0; e < PER; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = 0u;
+        if (p.lse && lane == 0) p.lse[(static_cast<size_t>(b) * p.N + i) * p.Hq + h] = -INFINITY;
+        return;
+    }
+    const size_t slot0 = (static_cast<size_t>(b) * p.Hkv + kvh) * p.max_chunks;
+    const float2* ml = p.ws_ml + slot0 * p.R + r;            // chunk c at ml[c * R]
+    const float* o_row = p.ws_o + (slot0 * p.R + r) * DH + lane * PER;
+    const size_t o_stride = static_cast<size_t>(p.R) * DH;   // one chunk
+    // the first batch of vectors and every chunk's (max, sum), all in flight together
+    VecT v[kMergeBatch];
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k)
+        if (k < nchunks) v[k] = *reinterpret_cast<const VecT*>(o_row + static_cast<size_t>(k) * o_stride);
+    float2 mlv[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const int c = lane + 32 * q;
+        mlv[q] = c < nchunks ? ml[static_cast<size_t>(c) * p.R] : make_float2(-INFINITY, 0.0f);
+    }
+    float M = fmaxf(mlv[0].x, mlv[1].x);
+    for (int c = lane + 64; c < nchunks; c += 32) M = fmaxf(M, ml[static_cast<size_t>(c) * p.R].x);
+    M = warp_max_f(M);
+    const float m_use = (M == -INFINITY) ? 0.0f : M;
+    // lane l holds the weights of chunks l and l + 32
+    const float w0 = exp2f(mlv[0].x - m_use), w1 = exp2f(mlv[1].x - m_use);
+    float lpart = mlv[0].y * w0 + mlv[1].y * w1;
+    for (int c = lane + 64; c < nchunks; c += 32) {
+        const float2 mv = ml[static_cast<size_t>(c) * p.R];
+        lpart += mv.y * exp2f(mv.x - m_use);
+    }
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.0f;
+    for (int c0 = 0; c0 < nchunks; c0 += kMergeBatch) {
+        if (c0 > 0) {
+#pragma unroll
+            for (int k = 0; k < kMergeBatch; ++k)
+                if (c0 + k < nchunks) v[k] = *reinterpret_cast<const VecT*>(o_row + static_cast<size_t>(c0 + k) * o_stride);
+        }
+        // a batch lies within chunks [0, 32) or [32, 64) (kMergeBatch divides 32)
+        const float wsel = c0 < 32 ? w0 : w1;
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            const int c = c0 + k;
+            float w;
+            if (c0 < 64) w = __shfl_sync(0xffffffffu, wsel, c & 31);
+            else w = c < nchunks ? exp2f(ml[static_cast<size_t>(c) * p.R].x - m_use) : 0.0f;
+            if (c < nchunks) {
+                if constexpr (PER == 4) {
+                    acc[0] += v[k].x * w; acc[1] += v[k].y * w; acc[2] += v[k].z * w; acc[3] += v[k].w * w;
+                } else {
+                    acc[0] += v[k].x * w; acc[1] += v[k].y * w;
+                }
+            }
+        }
+    }
+    const float lsum = warp_sum_f(lpart);
+    const bool real = i < nn;
+    const float inv = (real && lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+        *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    if (p.lse && lane == 0)
+        p.lse[(static_cast<size_t>(b) * p.N + i) * p.Hq + h] =
+            (real && lsum > 0.0f) ? (M + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
+}
+
 template <int DH>
 static cudaError_t launch_dh(const AttnParams& p, cudaStream_t stream) {
     using T = MmaTile<DH>;
@@ -394,8 +495,13 @@ cudaError_t launch_attn_mma(const AttnParams& p, cudaStream_t stream) {
 cudaError_t launch_attn_combine(const AttnParams& p, cudaStream_t stream) {
     if (p.max_chunks <= 1) return cudaSuccess;
     const dim3 g2((p.R + 7) / 8, p.Hkv, p.B);
-    if (p.Dh == 128) attn_combine_kernel<128><<<g2, 256, 0, stream>>>(p);
-    else attn_combine_kernel<64><<<g2, 256, 0, stream>>>(p);
+    if (p.merge_wide) {
+        if (p.Dh == 128) attn_combine_wide_kernel<128><<<g2, 256, 0, stream>>>(p);
+        else attn_combine_wide_kernel<64><<<g2, 256, 0, stream>>>(p);
+    } else {
+        if (p.Dh == 128) attn_combine_kernel<128><<<g2, 256, 0, stream>>>(p);
+        else attn_combine_kernel<64><<<g2, 256, 0, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 
