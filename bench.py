@@ -44,7 +44,8 @@ METRIC = "tree-verify steps/s & attn HBM GB/s (% roofline), batch16 ctx8k budget
 # dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture (a metric
 # list, one launch) of `bench.py --steps 5 --warmup 3 --no-cpu-baseline
 # --e2e-steps 3`, on the current kernel (profiles/attn_tc_batched16_ctx8k.md).
-ATTN_TC_TRAFFIC_BYTES = 533646848 + 25419264
+ATTN_TC_TRAFFIC_BYTES = 533681664 + 25398016
+L2_FLUSH_BELOW = 256e6   # a paged KV cache smaller than this is timed with L2 flushed
 WORKLOAD_DESC = ("batched serving: 16 requests, ctx ~U[1024,16384] paged (page 64, shuffled), "
                  "Hq 64 / Hkv 8 / Dh 128 bf16, budget 32 (N=33), top-k 8, depth 8, vocab 32000")
 
@@ -542,8 +543,36 @@ def run_native(args):
         "ddtree_accept_sample_ratio": lambda: dd.ddtree_accept_sample_ratio(logits, dl_d, tree, w.D, temp, seed,
                                                                             0, out=ro, dev_status=status),
     }
-    call_graphs = {n: graph_of(f, 10) for n, f in calls.items()}
+    # A workload whose paged KV cache fits in L2 is timed one step at a time with
+    # L2 flushed (a 256 MB write, outside the timed events) before every step;
+    # larger ones run back to back (their inputs exceed L2).
+    kv_bytes = h["kv"]["k_cache"].nbytes * 2
+    flush_l2 = kv_bytes < L2_FLUSH_BELOW
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=device) if flush_l2 else None
+    reps = 1 if flush_l2 else 10
+    call_graphs = {n: graph_of(f, reps) for n, f in calls.items()}
     torch.cuda.synchronize()
+
+    def time_replays(gr, n):
+        """Milliseconds of n replays of gr on `stream`: one event pair around all of
+        them, or, with L2 flushed, one pair per replay (the flush outside)."""
+        if not flush_l2:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(n):
+                gr.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for k, (e0, e1) in enumerate(evs):
+            flush_buf.fill_(k & 255)
+            e0.record(stream)
+            gr.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return sum(e0.elapsed_time(e1) for e0, e1 in evs)
 
     def barrier():
         if world > 1:
@@ -557,49 +586,41 @@ def run_native(args):
     with ClockSampler(local, args.clocks_dir) as clk:
         torch.cuda.synchronize()
         barrier()
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        t_end.record(stream)
-        torch.cuda.synchronize()
+        elapsed_ms = time_replays(graph, args.steps)
         barrier()
-        # tree_verify_attn alone, back to back on the same stream (roofline timing)
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        attn_reps = max(20, args.steps // 10)
-        a0.record(stream)
-        for _ in range(attn_reps // 10):
-            call_graphs["tree_verify_attn"].replay()
-        a1.record(stream)
-        torch.cuda.synchronize()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    attn_avg_ms = a0.elapsed_time(a1) / ((attn_reps // 10) * 10)
+        # tree_verify_attn alone on the same stream (roofline timing)
+        attn_calls = max(20, args.steps // 10) // 10 * 10
+        attn_avg_ms = time_replays(call_graphs["tree_verify_attn"], attn_calls // reps) / attn_calls
     per_call_us = {}
     for n, gr in call_graphs.items():
         gr.replay()
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(5):
-            gr.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        per_call_us[n] = e0.elapsed_time(e1) * 1e3 / 50
+        per_call_us[n] = time_replays(gr, 50 // reps) * 1e3 / 50
     # the library's step graph, launched directly (a graph launch per step)
     for _ in range(3):
         native_step.launch()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(50):
-        native_step.launch()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    per_call_us["ddtree_step_graph"] = e0.elapsed_time(e1) * 1e3 / 50
+    if flush_l2:
+        step_ms = 0.0
+        for k in range(50):
+            flush_buf.fill_(k & 255)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            native_step.launch()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            step_ms += e0.elapsed_time(e1)
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(50):
+            native_step.launch()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        step_ms = e0.elapsed_time(e1)
+    per_call_us["ddtree_step_graph"] = step_ms * 1e3 / 50
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
@@ -701,8 +722,10 @@ def run_native(args):
             "config": {"workload": WORKLOAD_DESC if w.name == "batched" else w.name,
                        "global_batch": w.B * world, "seq_len": mean_context(w),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (paged KV cache %.0f MB > 129 MB L2)"
-                             % (h["kv"]["k_cache"].nbytes * 2 / 1e6)},
+                       "l2": (("L2 flushed before every timed step (256 MB write outside the events; "
+                               "paged KV cache %.0f MB < 129 MB L2; the e2e leg is not flushed)" % (kv_bytes / 1e6))
+                              if flush_l2 else
+                              "inputs larger than L2 (paged KV cache %.0f MB > 129 MB L2)" % (kv_bytes / 1e6))},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak,
                          "traffic": ATTN_TC_TRAFFIC_BYTES if w.name == "batched" else None,
