@@ -745,40 +745,55 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             }
             // scale, mask; c0/c1: key kA rows crow0/crow0+1; c2/c3: key kA+8
             const int kA = 16 * sw + nrow;
+            if (ti.ctx && ti.valid == kKeys) {   // a full context tile: only rows past R are masked
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                c[e] += c2[e];
-                const int kl = kA + ((e >> 1) << 3);
-                const int q = e & 1;
-                bool vis_ok = node_r[q] >= 0 && kl < ti.valid;
-                if (!ti.ctx && vis_ok) {
-                    const int key = ti.key0 + kl;
-                    vis_ok = (pick4(visr[q], key >> 5) >> (key & 31)) & 1u;
+                for (int e = 0; e < 4; ++e) {
+                    c[e] += c2[e];
+                    c[e] = node_r[e & 1] >= 0 ? c[e] * p.scale_log2 : -INFINITY;
                 }
-                c[e] = vis_ok ? c[e] * p.scale_log2 : -INFINITY;
-            }
-            float mx[2] = {fmaxf(c[0], c[2]), fmaxf(c[1], c[3])};
-            float alpha[2], m_use[2];
+            } else {
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 4));
-                mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 8));
-                mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 16));
-                const float m_new = fmaxf(m_run[q], mx[q]);
-                m_use[q] = (m_new == -INFINITY) ? 0.0f : m_new;
-                alpha[q] = fast_exp2(m_run[q] - m_use[q]);
-                m_run[q] = m_new;
+                for (int e = 0; e < 4; ++e) {
+                    c[e] += c2[e];
+                    const int kl = kA + ((e >> 1) << 3);
+                    const int q = e & 1;
+                    bool vis_ok = node_r[q] >= 0 && kl < ti.valid;
+                    if (!ti.ctx && vis_ok) {
+                        const int key = ti.key0 + kl;
+                        vis_ok = (pick4(visr[q], key >> 5) >> (key & 31)) & 1u;
+                    }
+                    c[e] = vis_ok ? c[e] * p.scale_log2 : -INFINITY;
+                }
             }
+            // Lazy rescale, as for the main rows: the reference max of a row moves
+            // only when a score exceeds it by more than 2^8; most tiles then need
+            // neither the row max nor a rescale of the accumulators.
+            const bool up = fmaxf(c[0], c[2]) > m_run[0] + 8.0f || fmaxf(c[1], c[3]) > m_run[1] + 8.0f;
+            float alpha[2] = {1.0f, 1.0f};
+            if (__any_sync(0xffffffffu, up)) {
+                float mx[2] = {fmaxf(c[0], c[2]), fmaxf(c[1], c[3])};
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 4));
+                    mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 8));
+                    mx[q] = fmaxf(mx[q], __shfl_xor_sync(0xffffffffu, mx[q], 16));
+                    if (mx[q] > m_run[q] + 8.0f) {
+                        alpha[q] = m_run[q] == -INFINITY ? 1.0f : fast_exp2(m_run[q] - mx[q]);
+                        m_run[q] = mx[q];
+                    }
+                }
+#pragma unroll
+                for (int mb = 0; mb < kD / 16; ++mb) {
+                    oacc[mb][0] *= alpha[0]; oacc[mb][2] *= alpha[0];
+                    oacc[mb][1] *= alpha[1]; oacc[mb][3] *= alpha[1];
+                }
+            }
+            const float m_use[2] = {m_run[0] == -INFINITY ? 0.0f : m_run[0], m_run[1] == -INFINITY ? 0.0f : m_run[1]};
             float pe[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) pe[e] = fast_exp2(c[e] - m_use[e & 1]);
             l_part[0] = l_part[0] * alpha[0] + pe[0] + pe[2];
             l_part[1] = l_part[1] * alpha[1] + pe[1] + pe[3];
-#pragma unroll
-            for (int mb = 0; mb < kD / 16; ++mb) {
-                oacc[mb][0] *= alpha[0]; oacc[mb][2] *= alpha[0];
-                oacc[mb][1] *= alpha[1]; oacc[mb][3] *= alpha[1];
-            }
             __nv_bfloat162 p01 = __floats2bfloat162_rn(pe[0], pe[1]);
             __nv_bfloat162 p23 = __floats2bfloat162_rn(pe[2], pe[3]);
             const uint32_t b0 = movmatrix_t(*reinterpret_cast<uint32_t*>(&p01));
