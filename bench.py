@@ -1,9 +1,11 @@
 """Benchmark of the DDTree tree-verify step on GB300.
 
 One step = the whole hot path over one batch: ddtree_build -> tree_verify_attn
--> ddtree_accept_greedy and ddtree_accept_sample (the sampled walk runs on the
-same tree at T = 0.7, as a server would for the temperature requests of a
-batch; the two walks are independent and run concurrently on two streams).
+-> the greedy and the temperature walk (the sampled walk runs on the same tree
+at T = 0.7, as a server would for the temperature requests of a batch; both
+walks run in one launch, ddtree_accept_greedy_sample, whose outputs equal the
+separate ddtree_accept_greedy and ddtree_accept_sample calls; those two are
+timed on their own as well).
 The step's input, the per-depth top-k, is made once by ddtree_draft_topk
 from the draft logits; that call, the draft-ratio walk
 (ddtree_accept_sample_ratio), ddtree_commit_kv and the library's own step
@@ -484,20 +486,14 @@ def run_native(args):
     ro = {k: torch.empty_like(t) for k, t in go.items()}
     scale = 1.0 / math.sqrt(w.Dh)
 
-    walk_stream = torch.cuda.Stream(device)
-
     def step():
         dd.ddtree_build(topk_logp, topk_tok, root, ctx, w.budget, out=tree, dev_status=status)
         dd.tree_verify_attn(q, k_tree, v_tree, k_cache, v_cache, table, ctx, tree.vis, tree.n_nodes,
                             scale, out=out, workspace=workspace, dev_status=status)
-        # the two walks read the same tree and logits and write separate outputs:
-        # the sampled walk runs on a second stream, concurrently with the greedy one
-        cur = torch.cuda.current_stream()
-        walk_stream.wait_stream(cur)
-        dd.ddtree_accept_greedy(logits, tree, w.D, out=go, dev_status=status)
-        with torch.cuda.stream(walk_stream):
-            dd.ddtree_accept_sample(logits, tree, w.D, temp, seed, 0, out=so, dev_status=status)
-        cur.wait_stream(walk_stream)
+        # the greedy and the temperature walk of the tree, in one launch (outputs
+        # identical to the two separate calls, which the GPU does not overlap)
+        dd.ddtree_accept_greedy_sample(logits, tree, w.D, temp, seed, 0, out_greedy=go, out_sample=so,
+                                       dev_status=status)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -540,6 +536,9 @@ def run_native(args):
         "ddtree_accept_greedy": lambda: dd.ddtree_accept_greedy(logits, tree, w.D, out=go, dev_status=status),
         "ddtree_accept_sample": lambda: dd.ddtree_accept_sample(logits, tree, w.D, temp, seed, 0, out=so,
                                                                 dev_status=status),
+        "ddtree_accept_greedy_sample": lambda: dd.ddtree_accept_greedy_sample(logits, tree, w.D, temp, seed, 0,
+                                                                              out_greedy=go, out_sample=so,
+                                                                              dev_status=status),
         "ddtree_accept_sample_ratio": lambda: dd.ddtree_accept_sample_ratio(logits, dl_d, tree, w.D, temp, seed,
                                                                             0, out=ro, dev_status=status),
     }
@@ -582,7 +581,7 @@ def run_native(args):
         graph.replay()
     torch.cuda.synchronize()
     barrier()
-    launches_per_step = 4 + (1 if ws_bytes > 0 else 0)
+    launches_per_step = 3 + (1 if ws_bytes > 0 else 0)   # build, attention (+ merge), walks
     with ClockSampler(local, args.clocks_dir) as clk:
         torch.cuda.synchronize()
         barrier()
@@ -647,13 +646,9 @@ def run_native(args):
                         dev_status=status)
         dd.tree_verify_attn(di["q"], di["k_tree"], di["v_tree"], k_cache, v_cache, di["table"], di["ctx"],
                             tree.vis, tree.n_nodes, scale, out=do["out"], workspace=workspace, dev_status=status)
-        cur = torch.cuda.current_stream()
-        walk_stream.wait_stream(cur)
-        dd.ddtree_accept_greedy(di["logits"], tree, w.D, out={k: do[f"g_{k}"] for k in go}, dev_status=status)
-        with torch.cuda.stream(walk_stream):
-            dd.ddtree_accept_sample(di["logits"], tree, w.D, di["temp"], di["seed"], 0,
-                                    out={k: do[f"s_{k}"] for k in so}, dev_status=status)
-        cur.wait_stream(walk_stream)
+        dd.ddtree_accept_greedy_sample(di["logits"], tree, w.D, di["temp"], di["seed"], 0,
+                                       out_greedy={k: do[f"g_{k}"] for k in go},
+                                       out_sample={k: do[f"s_{k}"] for k in so}, dev_status=status)
 
     set_graphs = []
     for di, do in sets:

@@ -311,6 +311,41 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                          int32_t* dev_status, void* stream);
 
 /*
+ * ddtree_accept_greedy_sample - ddtree_accept_greedy and ddtree_accept_sample
+ * of the same tree and logits in one launch.
+ *
+ * [Arch] Section 1 step 5 and Section 3: the two walks are the ones the two
+ * calls above make; this entry point runs them side by side, one round per
+ * tree level, so that both share each round's synchronisation and, while
+ * they stand on the same node, its logits row. The pages have no such call:
+ * it exists because a verify step that needs both results (a serving loop
+ * that verifies greedy and sampled requests of one batch, or a caller that
+ * reports both) would otherwise pay two latency-bound launches that do not
+ * overlap on the GPU.
+ *
+ * Inputs: as ddtree_accept_sample (temperature, seed and philox_offset are
+ * used by the temperature walk only).
+ * Outputs: greedy_* as ddtree_accept_greedy's outputs, sample_* as
+ * ddtree_accept_sample's (both *_walk_stats and sample_margin_stats
+ * nullable); every output is bit-identical to the one the separate call
+ * writes for the same inputs. Device errors: the union of the two calls'.
+ * Errors: as the two calls (the same argument checks, applied to both output
+ * sets).
+ */
+int ddtree_accept_greedy_sample(const float* logits, int V, const int32_t* token,
+                                const int32_t* first_child, const int32_t* next_sibling,
+                                const int32_t* n_nodes, int B, int N, int D,
+                                const float* temperature, const uint64_t* seed,
+                                uint64_t philox_offset,
+                                int32_t* greedy_accept_len, int32_t* greedy_out_tokens,
+                                int32_t* greedy_out_nodes, int32_t* greedy_bonus,
+                                int32_t* greedy_walk_stats,
+                                int32_t* sample_accept_len, int32_t* sample_out_tokens,
+                                int32_t* sample_out_nodes, int32_t* sample_bonus,
+                                float* sample_margin_stats, int32_t* sample_walk_stats,
+                                int32_t* dev_status, void* stream);
+
+/*
  * ddtree_accept_sample_ratio - the temperature walk with the draft-ratio rule.
  *
  * [Arch] Section 3 (linear case: accept draft token t with probability

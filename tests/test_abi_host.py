@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_four_calls():
     names = declared_functions()
-    for n in ("ddtree_draft_topk", "ddtree_commit_kv", "ddtree_accept_sample_ratio", "ddtree_build", "tree_verify_attn", "ddtree_accept_greedy", "ddtree_accept_sample"):
+    for n in ("ddtree_draft_topk", "ddtree_commit_kv", "ddtree_accept_sample_ratio", "ddtree_build", "tree_verify_attn",
+              "ddtree_accept_greedy", "ddtree_accept_sample", "ddtree_accept_greedy_sample"):
         assert n in names
 
 
@@ -189,6 +190,26 @@ def test_ratio_walk_rejects_bad_arguments(lib, kw, code):
 
 def test_ratio_walk_empty_batch_is_a_noop(lib):
     assert lib.ddtree_accept_sample_ratio(*ratio_args(B=0, logits=0, draft=0)) == 0
+
+
+def both_args(**kw):
+    a = dict(logits=FAKE, V=100, token=FAKE, fc=FAKE, ns=FAKE, nn=FAKE, B=2, N=33, D=8, temp=FAKE,
+             seed=FAKE, offset=0, g_acc=FAKE, g_toks=FAKE, g_nodes=FAKE, g_bonus=FAKE, g_stats=0,
+             s_acc=FAKE, s_toks=FAKE, s_nodes=FAKE, s_bonus=FAKE, s_margin=0, s_stats=0, status=0, stream=0)
+    a.update(kw)
+    return [a[k] for k in ("logits", "V", "token", "fc", "ns", "nn", "B", "N", "D", "temp", "seed", "offset",
+                           "g_acc", "g_toks", "g_nodes", "g_bonus", "g_stats", "s_acc", "s_toks", "s_nodes",
+                           "s_bonus", "s_margin", "s_stats", "status", "stream")]
+
+
+@pytest.mark.parametrize("kw,code", [(dict(V=0), -1), (dict(N=200), -2), (dict(D=0), -2), (dict(D=65), -2),
+                                     (dict(logits=0), -1), (dict(token=0), -1), (dict(g_bonus=0), -1),
+                                     (dict(s_bonus=0), -1), (dict(g_nodes=0), -1), (dict(s_acc=0), -1),
+                                     (dict(temp=0), -1), (dict(seed=0), -1), (dict(offset=1 << 56), -1),
+                                     (dict(B=0, logits=0), 0)])
+def test_fused_walks_reject_bad_arguments(lib, kw, code):
+    # the checks of the two separate calls, on both output sets; nothing launches
+    assert lib.ddtree_accept_greedy_sample(*both_args(**kw)) == code
 
 
 def test_sample_rejects_missing_rng_inputs_and_large_offset(lib):

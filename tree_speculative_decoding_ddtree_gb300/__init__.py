@@ -20,6 +20,7 @@ from . import _build
 __all__ = [
     "DDTreeError", "load_library", "library_path", "ddtree_draft_topk", "ddtree_build", "tree_verify_attn",
     "tree_verify_attn_workspace_size", "ddtree_accept_greedy", "ddtree_accept_sample",
+    "ddtree_accept_greedy_sample",
     "TreeBuffers", "alloc_tree", "DEV_ERRORS", "tree_verify_attn_noalloc", "ddtree_commit_kv",
     "StepArgs", "VerifyStep", "ddtree_accept_sample_ratio",
 ]
@@ -83,6 +84,8 @@ def load_library(path: Optional[str] = None):
     lib.ddtree_accept_greedy.argtypes = [P, I, P, P, P, P, I, I, I, P, P, P, P, P, P, P]
     lib.ddtree_accept_sample.restype = I
     lib.ddtree_accept_sample.argtypes = [P, I, P, P, P, P, I, I, I, P, P, U64, P, P, P, P, P, P, P, P]
+    lib.ddtree_accept_greedy_sample.argtypes = [P, I, P, P, P, P, I, I, I, P, P, U64, P, P, P, P, P,
+                                                P, P, P, P, P, P, P, P]
     if path is None:
         _lib = lib
     return lib
@@ -373,6 +376,44 @@ def ddtree_accept_sample(logits: torch.Tensor, tree: TreeBuffers, D: int,
         _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
     _check(st, "ddtree_accept_sample")
     return o
+
+
+def ddtree_accept_greedy_sample(logits: torch.Tensor, tree: TreeBuffers, D: int,
+                                temperature: torch.Tensor, seed: torch.Tensor, philox_offset: int,
+                                out_greedy=None, out_sample=None,
+                                dev_status: Optional[torch.Tensor] = None, stream=None,
+                                greedy_walk_stats: Optional[torch.Tensor] = None,
+                                sample_margin_stats: Optional[torch.Tensor] = None,
+                                sample_walk_stats: Optional[torch.Tensor] = None):
+    """The greedy and the temperature walk in one launch (see
+    ``ddtree_accept_greedy_sample`` in include/ddtree.h); returns the two output
+    dicts, each identical to what the separate call writes."""
+    lib = load_library()
+    B, N, V = logits.shape
+    og = _walk_outputs(B, D, logits.device, out_greedy)
+    os_ = _walk_outputs(B, D, logits.device, out_sample)
+    st = lib.ddtree_accept_greedy_sample(
+        _ptr(logits, torch.float32, "logits", (B, N, V)), V,
+        _ptr(tree.token, torch.int32, "token", (B, N)),
+        _ptr(tree.first_child, torch.int32, "first_child", (B, N)),
+        _ptr(tree.next_sibling, torch.int32, "next_sibling", (B, N)),
+        _ptr(tree.n_nodes, torch.int32, "n_nodes", (B,)), B, N, D,
+        _ptr(temperature, torch.float32, "temperature", (B,)),
+        _ptr(seed, torch.int64, "seed", (B,)), int(philox_offset),
+        _ptr(og["accept_len"], torch.int32, "greedy accept_len", (B,)),
+        _ptr(og["out_tokens"], torch.int32, "greedy out_tokens", (B, D + 1)),
+        _ptr(og["out_nodes"], torch.int32, "greedy out_nodes", (B, D + 1)),
+        _ptr(og["bonus"], torch.int32, "greedy bonus", (B,)),
+        _ptr(greedy_walk_stats, torch.int32, "greedy_walk_stats", (B, 4)),
+        _ptr(os_["accept_len"], torch.int32, "sample accept_len", (B,)),
+        _ptr(os_["out_tokens"], torch.int32, "sample out_tokens", (B, D + 1)),
+        _ptr(os_["out_nodes"], torch.int32, "sample out_nodes", (B, D + 1)),
+        _ptr(os_["bonus"], torch.int32, "sample bonus", (B,)),
+        _ptr(sample_margin_stats, torch.float32, "sample_margin_stats", (B,)),
+        _ptr(sample_walk_stats, torch.int32, "sample_walk_stats", (B, 4)),
+        _ptr(dev_status, torch.int32, "dev_status", (1,)), _stream(stream))
+    _check(st, "ddtree_accept_greedy_sample")
+    return og, os_
 
 
 def tree_verify_attn_noalloc(q: torch.Tensor, k_tree: torch.Tensor, v_tree: torch.Tensor,

@@ -9,6 +9,7 @@
 #include "common.cuh"
 #include "ddtree_testing.h"
 #include "trace.h"
+#include "walk.cuh"
 
 namespace ddt {
 cudaError_t launch_build(const float*, const int32_t*, const int32_t*, const int32_t*, int, int,
@@ -21,6 +22,9 @@ cudaError_t launch_accept_sample(const float*, int, const int32_t*, const int32_
                                  const int32_t*, const int32_t*, int, int, int, const float*,
                                  const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*,
                                  int32_t*, float*, int32_t*, int32_t*, cudaStream_t);
+cudaError_t launch_accept_both(const float*, int, const int32_t*, const int32_t*, const int32_t*,
+                               const int32_t*, int, int, int, const float*, const uint64_t*, uint64_t,
+                               const WalkOut&, const WalkOut&, int32_t*, cudaStream_t);
 cudaError_t launch_draft_topk(const float*, int, int, int, int, float*, int32_t*, cudaStream_t);
 cudaError_t launch_accept_ratio(const float*, const float*, int, const int32_t*, const int32_t*,
                                 const int32_t*, const int32_t*, int, int, int, const float*,
@@ -309,6 +313,34 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
                                          N, D, temperature, seed, philox_offset, accept_len,
                                          out_tokens, out_nodes, bonus, margin_stats, walk_stats,
                                          dev_status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
+}
+
+int ddtree_accept_greedy_sample(const float* logits, int V, const int32_t* token,
+                                const int32_t* first_child, const int32_t* next_sibling,
+                                const int32_t* n_nodes, int B, int N, int D, const float* temperature,
+                                const uint64_t* seed, uint64_t philox_offset,
+                                int32_t* greedy_accept_len, int32_t* greedy_out_tokens,
+                                int32_t* greedy_out_nodes, int32_t* greedy_bonus, int32_t* greedy_walk_stats,
+                                int32_t* sample_accept_len, int32_t* sample_out_tokens,
+                                int32_t* sample_out_nodes, int32_t* sample_bonus, float* sample_margin_stats,
+                                int32_t* sample_walk_stats, int32_t* dev_status, void* stream) {
+    TraceRange trace("ddtree_accept_greedy_sample");
+    int st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
+                             greedy_accept_len, greedy_out_tokens, greedy_out_nodes, greedy_bonus);
+    if (st != DDT_OK) return st;
+    st = check_walk_args(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
+                         sample_accept_len, sample_out_tokens, sample_out_nodes, sample_bonus);
+    if (st != DDT_OK || B == 0) return st;
+    if (!temperature || !seed) return DDT_EINVAL;
+    if (philox_offset >> 56) return DDT_EINVAL;
+    const WalkOut og{greedy_accept_len, greedy_out_tokens, greedy_out_nodes, greedy_bonus, nullptr,
+                     greedy_walk_stats};
+    const WalkOut os{sample_accept_len, sample_out_tokens, sample_out_nodes, sample_bonus, sample_margin_stats,
+                     sample_walk_stats};
+    cudaError_t e = launch_accept_both(logits, V, token, first_child, next_sibling, n_nodes, B, N, D,
+                                       temperature, seed, philox_offset, og, os, dev_status,
+                                       static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
 
