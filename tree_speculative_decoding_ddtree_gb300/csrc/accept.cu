@@ -152,6 +152,7 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         return;
     }
     const float inv_t = 1.0f / T;
+    const float s2 = inv_t * 1.4426950408889634f;   // log2(e) / T
     const uint64_t sd = seed[b];
     const uint32_t k0 = static_cast<uint32_t>(sd), k1 = static_cast<uint32_t>(sd >> 32);
     const uint32_t off_lo = static_cast<uint32_t>(offset);
@@ -187,58 +188,27 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
             const int x = s_kid_tok[threadIdx.x];
             s_kid_logit[threadIdx.x] = (x >= 0 && x < V) ? __ldg(row + x) : 0.0f;
         }
-        // this CTA's slice: running max and softmax denominator of logits / T
-        MaxSum ms{-INFINITY, 0.0f};
-        auto add = [&](float x) {
-            if (x > ms.m) {
-                ms.z = ms.z * expf((ms.m - x) * inv_t) + 1.0f;
-                ms.m = x;
-            } else {
-                ms.z += expf((x - ms.m) * inv_t);
-            }
-        };
+        // this CTA's slice: softmax statistics of logits / T in the exp2 domain
+        SMaxSum ms{-INFINITY, 0.0f};
         if (vec4) {
             const float4* r4 = reinterpret_cast<const float4*>(row);
 #pragma unroll 4
-            for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads) {
-                const float4 f = __ldg(r4 + x);
-                add(f.x); add(f.y); add(f.z); add(f.w);
-            }
+            for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads)
+                sms_add4(ms, __ldg(r4 + x), s2);
         } else {
-            for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads) add(__ldg(row + v));
+            for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads)
+                sms_add1(ms, __ldg(row + v), s2);
         }
-        {
-            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
-                ms = merge_ms(ms, other, inv_t);
-            }
-            __syncthreads();
-            if (lane == 0) { scratch_m[warp] = ms.m; scratch_z[warp] = ms.z; }
-            __syncthreads();
-            if (warp == 0) {
-                ms.m = lane < kWalkThreads / 32 ? scratch_m[lane] : -INFINITY;
-                ms.z = lane < kWalkThreads / 32 ? scratch_z[lane] : 0.0f;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
-                    ms = merge_ms(ms, other, inv_t);
-                }
-                if (lane == 0) part_ms[level & 1] = make_float2(ms.m, ms.z);
-            }
-        }
+        ms = sms_block(ms, scratch_m, scratch_z);
+        if (threadIdx.x == 0) part_ms[level & 1] = make_float2(ms.m, ms.z);
         cluster_barrier();
-        if (threadIdx.x == 0) {
-            // the same partials merged in the same order in every CTA
-            MaxSum acc{-INFINITY, 0.0f};
-#pragma unroll
-            for (int r = 0; r < kCluster; ++r) {
-                const float2 pr = ld_cluster_f32x2(cluster_addr(&part_ms[level & 1], r));
-                acc = merge_ms(acc, MaxSum{pr.x, pr.y}, inv_t);
+        if (threadIdx.x < 32) {
+            // the same partials merged by the same shuffle tree in every CTA
+            const SMaxSum acc = sms_cluster(&part_ms[level & 1]);
+            if (threadIdx.x == 0) {
+                s_m = acc.m;
+                s_z = acc.z;
             }
-            s_m = acc.m;
-            s_z = acc.z;
         }
         __syncthreads();
         // child j: q(x_j) and its uniform, one thread each
@@ -246,7 +216,7 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
             const int j = threadIdx.x;
             const int x = s_kid_tok[j];
             float q = 0.0f;
-            if (x >= 0 && x < V) q = expf((s_kid_logit[j] - s_m) * inv_t) / s_z;
+            if (x >= 0 && x < V) q = ex2_approx(fmaf(s_kid_logit[j], s2, -s_m)) / s_z;
             else if (writer) report(dev_status, DDT_DEV_BAD_TOKEN);
             const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(u),
                                                      static_cast<uint32_t>(j), off_lo), k0, k1);

@@ -73,6 +73,7 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
     const float T = temperature[b];
     const bool t_ok = (T > 0.0f) && isfinite(T);   // the same decision in every CTA of the cluster
     const float inv_t = t_ok ? 1.0f / T : 1.0f;
+    const float s2 = inv_t * 1.4426950408889634f;   // log2(e) / T
     const uint64_t sd = seed[b];
     const uint32_t k0 = static_cast<uint32_t>(sd), k1 = static_cast<uint32_t>(sd >> 32);
     const uint32_t off_lo = static_cast<uint32_t>(offset);
@@ -132,15 +133,7 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
         if (g_on || s_walk) {
             const bool same = g_on && s_walk && ug == us;
             unsigned long long best = 0ull;
-            MaxSum ms{-INFINITY, 0.0f};
-            auto add = [&](float x) {
-                if (x > ms.m) {
-                    ms.z = ms.z * expf((ms.m - x) * inv_t) + 1.0f;
-                    ms.m = x;
-                } else {
-                    ms.z += expf((x - ms.m) * inv_t);
-                }
-            };
+            SMaxSum ms{-INFINITY, 0.0f};
             auto arg = [&](float f, uint32_t v) {
                 const unsigned long long pk = argmax_pack(float_order_key(f), v);
                 return pk;
@@ -162,7 +155,7 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
                         p0 = p0 > p2 ? p0 : p2;
                         best = best > p0 ? best : p0;
                     }
-                    if (s_walk) { add(fs.x); add(fs.y); add(fs.z); add(fs.w); }
+                    if (s_walk) sms_add4(ms, fs, s2);
                 }
             } else {
                 for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads) {
@@ -173,7 +166,7 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
                         const unsigned long long p = arg(fg, static_cast<uint32_t>(v));
                         best = best > p ? best : p;
                     }
-                    if (s_walk) add(fs);
+                    if (s_walk) sms_add1(ms, fs, s2);
                 }
             }
             // both block reductions under one pair of barriers
@@ -182,8 +175,8 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
             for (int off = 16; off > 0; off >>= 1) {
                 const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, off);
                 best = best > ob ? best : ob;
-                MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
-                ms = merge_ms(ms, other, inv_t);
+                ms = sms_merge(ms, SMaxSum{__shfl_xor_sync(0xffffffffu, ms.m, off),
+                                           __shfl_xor_sync(0xffffffffu, ms.z, off)});
             }
             __syncthreads();
             if (lane == 0) { scratch_a[warp] = best; scratch_m[warp] = ms.m; scratch_z[warp] = ms.z; }
@@ -196,8 +189,8 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
                 for (int off = 16; off > 0; off >>= 1) {
                     const unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, off);
                     best = best > ob ? best : ob;
-                    MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
-                    ms = merge_ms(ms, other, inv_t);
+                    ms = sms_merge(ms, SMaxSum{__shfl_xor_sync(0xffffffffu, ms.m, off),
+                                               __shfl_xor_sync(0xffffffffu, ms.z, off)});
                 }
                 if (lane == 0) {
                     if (g_on) part_a[par] = best;
@@ -281,16 +274,13 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
             s_gnext = match;
         }
         if (s_walk) {
-            if (threadIdx.x == 0) {
-                // the same partials merged in the same order in every CTA
-                MaxSum acc{-INFINITY, 0.0f};
-#pragma unroll
-                for (int r = 0; r < kCluster; ++r) {
-                    const float2 pr = ld_cluster_f32x2(cluster_addr(&part_ms[par], r));
-                    acc = merge_ms(acc, MaxSum{pr.x, pr.y}, inv_t);
+            if (threadIdx.x < 32) {
+                // the same partials merged by the same shuffle tree in every CTA
+                const SMaxSum acc = sms_cluster(&part_ms[par]);
+                if (threadIdx.x == 0) {
+                    s_m = acc.m;
+                    s_z = acc.z;
                 }
-                s_m = acc.m;
-                s_z = acc.z;
             }
             __syncthreads();
             // child j: q(x_j) and its uniform, one thread each
@@ -298,7 +288,7 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
                 const int j = threadIdx.x;
                 const int x = s_kid_tok[j];
                 float q = 0.0f;
-                if (x >= 0 && x < V) q = expf((s_kid_logit[j] - s_m) * inv_t) / s_z;
+                if (x >= 0 && x < V) q = ex2_approx(fmaf(s_kid_logit[j], s2, -s_m)) / s_z;
                 else if (writer) report(dev_status, DDT_DEV_BAD_TOKEN);
                 const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(us),
                                                          static_cast<uint32_t>(j), off_lo), k0, k1);

@@ -246,5 +246,79 @@ DDT_DEVINL MaxSum merge_ms(MaxSum a, MaxSum b, float inv_t) {
     return r;
 }
 
+// ---------------------------------------------------------------------------
+// The temperature walk's softmax statistics of a row in the exp2 domain:
+// m = the largest x * s (s = log2(e) / T > 0, the rounded product), z = the
+// sum over the row of 2^(x * s - m), each exponent one fused multiply-add
+// (so its error is relative to the difference, as for exp((x - max) / T))
+// and each power one ex2.approx. Merges and the children's probabilities use
+// the same units: q(x) = 2^(x * s - m) / z.
+// ---------------------------------------------------------------------------
+DDT_DEVINL float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+struct SMaxSum {
+    float m, z;
+};
+DDT_DEVINL SMaxSum sms_merge(SMaxSum a, SMaxSum b) {
+    const float M = fmaxf(a.m, b.m);
+    if (M == -INFINITY) return SMaxSum{-INFINITY, 0.0f};
+    return SMaxSum{M, a.z * ex2_approx(a.m - M) + b.z * ex2_approx(b.m - M)};
+}
+// four elements at a time: one rescale at most, four fused exponents
+DDT_DEVINL void sms_add4(SMaxSum& a, float4 f, float s) {
+    const float mx = fmaxf(fmaxf(f.x, f.y), fmaxf(f.z, f.w)) * s;
+    if (mx > a.m) {
+        a.z = a.z * ex2_approx(a.m - mx);
+        a.m = mx;
+    }
+    if (a.m == -INFINITY) return;
+    a.z += (ex2_approx(fmaf(f.x, s, -a.m)) + ex2_approx(fmaf(f.y, s, -a.m))) +
+           (ex2_approx(fmaf(f.z, s, -a.m)) + ex2_approx(fmaf(f.w, s, -a.m)));
+}
+DDT_DEVINL void sms_add1(SMaxSum& a, float f, float s) {
+    const float mx = f * s;
+    if (mx > a.m) {
+        a.z = a.z * ex2_approx(a.m - mx);
+        a.m = mx;
+    }
+    if (a.m == -INFINITY) return;
+    a.z += ex2_approx(fmaf(f, s, -a.m));
+}
+// block-wide merge over kWalkThreads threads (fixed shuffle tree); warp 0 holds the result
+DDT_DEVINL SMaxSum sms_block(SMaxSum ms, float* scratch_m, float* scratch_z) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        ms = sms_merge(ms, SMaxSum{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)});
+    __syncthreads();
+    if (lane == 0) { scratch_m[warp] = ms.m; scratch_z[warp] = ms.z; }
+    __syncthreads();
+    if (warp == 0) {
+        ms.m = lane < kWalkThreads / 32 ? scratch_m[lane] : -INFINITY;
+        ms.z = lane < kWalkThreads / 32 ? scratch_z[lane] : 0.0f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            ms = sms_merge(ms, SMaxSum{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)});
+    }
+    return ms;
+}
+// the cluster's partials (float2 `part` in every CTA), merged by a fixed
+// shuffle tree over lanes 0..kCluster-1 of warp 0 (call from all of warp 0);
+// every CTA gets the same result
+DDT_DEVINL SMaxSum sms_cluster(const float2* part) {
+    const int lane = threadIdx.x & 31;
+    SMaxSum ms{-INFINITY, 0.0f};
+    if (lane < kCluster) {
+        const float2 v = ld_cluster_f32x2(cluster_addr(part, static_cast<uint32_t>(lane)));
+        ms = SMaxSum{v.x, v.y};
+    }
+#pragma unroll
+    for (int off = kCluster / 2; off > 0; off >>= 1)
+        ms = sms_merge(ms, SMaxSum{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)});
+    return ms;
+}
 
 }  // namespace ddt
