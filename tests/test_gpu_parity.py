@@ -193,6 +193,11 @@ def test_attn_tiny_full():
     ([129, 4000], 128, 32, 8, 128, 64, 8, 16),      # 260 rows (4 leftover), page 128, two tree tiles
     ([2000], 32, 16, 2, 128, 32, 4, 6),             # 264 rows, page 32 (two page boxes per key tile)
     ([6000, 1], 16, 8, 8, 128, 127, 4, 9),          # MHA, N = 128: 128 rows, one tile, page 16
+    # tensor-core row groups of 256 rows per (request, KV head)
+    ([3000, 70], 64, 64, 8, 128, 64, 8, 9),         # 520 rows: 256 + (256 + 8 leftover)
+    ([2500, 5], 16, 64, 4, 128, 32, 8, 8),          # G = 16, 528 rows: 256 + 256 + 16
+    ([1200], 64, 32, 4, 128, 127, 4, 10),           # 1024 rows: four groups
+    ([900, 4000], 32, 16, 4, 128, 99, 6, 9),        # 400 rows: 256 + 144 (a partial second tile)
 ])
 def test_attn_ragged_shapes(ctx, page_size, Hq, Hkv, Dh, budget, K, D):
     w = S.Workload(name="ragged", B=len(ctx), D=D, V=300, K=K, budget=budget, Hq=Hq, Hkv=Hkv,

@@ -29,6 +29,8 @@ struct AttnParams {
     int rows_per_group, n_groups;
     int tiles_per_chunk, max_chunks;
     int merge_wide;      // split-KV merge with several chunk loads in flight per warp (few rows per SM)
+    int tc_groups;       // tensor-core path: row groups of 256 rows per (request, KV head); the last
+                         // group takes the rest (256 + up to 8 leftover rows, or fewer than 256)
     float scale_log2;
     uint64_t stall_ns;   // 0; else (testing entry point only) a wait that nothing completes, bounded by this limit
 };

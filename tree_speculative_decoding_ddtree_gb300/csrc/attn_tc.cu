@@ -95,12 +95,13 @@ struct TcShared {
     float side_m[kMaxSide];
     int map_cnt[kLptMaxB];    // work-item counts in rank order (the CTA's item lookup)
     int map_off[kLptMaxB];    // their exclusive prefix sums
-    int item[6];              // this CTA's (request, KV head, chunk, found, ctx_len, n_nodes)
+    int item[7];              // this CTA's (request, KV head, chunk, found, ctx_len, n_nodes, row group)
 };
 
 struct Geometry {
     int b, kvh, chunk, L, nn, nchunks, t_begin, n_ctx, n_tree, n_tiles;
     int R, G, n_main, n_side;
+    int grp, r0;              // row group and its first row (rows r0 .. r0 + R - 1 of the request's G * N)
     bool bad;
 };
 
@@ -166,7 +167,7 @@ DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* it
             r += (ks > key[q]) || (ks == key[q] && s2 < b);
         }
         rnk[q] = r;
-        if (b < p.B) cnt[r] = nch[q] * p.Hkv;
+        if (b < p.B) cnt[r] = nch[q] * p.Hkv * p.tc_groups;
     }
     __syncwarp();
     // exclusive prefix over the ranked counts (two entries per lane)
@@ -188,7 +189,7 @@ DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* it
         const int b = lane + 32 * q;
         if (b < p.B) {
             const int o = off[rnk[q]];
-            if (i >= o && i < o + nch[q] * p.Hkv) { hit = q; local = i - o; }
+            if (i >= o && i < o + nch[q] * p.Hkv * p.tc_groups) { hit = q; local = i - o; }
         }
     }
     const unsigned m = __ballot_sync(0xffffffffu, hit >= 0);
@@ -197,11 +198,12 @@ DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* it
         if (lane == src) {
             const int b = lane + 32 * hit;
             item[0] = b;
-            item[1] = local / nch[hit];
+            item[1] = local / (nch[hit] * p.tc_groups);
             item[2] = local % nch[hit];
             item[3] = 1;
             item[4] = Lq[hit];
             item[5] = nnq[hit];
+            item[6] = (local / nch[hit]) % p.tc_groups;
         }
     } else if (lane == 0) {
         item[3] = 0;
@@ -220,9 +222,15 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     // ---------------- set-up: barriers, descriptors, TMEM ----------------
     // None of it depends on the work item (every CTA has the same rows), so it
     // runs beside the item lookup, under one barrier.
+    // Barrier counts are the same in every CTA: the Q copy is acknowledged by the
+    // softmax warps of n_main_all tiles (those of a tile a short row group does
+    // not use arrive without work), and when the last row group has leftover
+    // rows the leftover-row warps of every CTA take part in the K/V ring.
+    const int n_main_all = p.R > 128 ? 2 : 1;
+    const bool side_all = p.R - 256 * (p.tc_groups - 1) > 256;
     {
-        const int n_main = p.R > 128 ? 2 : 1;
-        const bool side = p.R > 256;
+        const int n_main = n_main_all;
+        const bool side = side_all;
         if (tid == 64) {   // warp 2: idle during the lookup
             mbar_init(bar_addr(sh.q_full), 1);
             for (int s = 0; s < kStages; ++s) {
@@ -268,16 +276,19 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         g.chunk = sh.item[2];
         g.L = sh.item[4];
         nn_loaded = sh.item[5];
-    } else {   // one-dimensional grid in (request, head, chunk) order
+        g.grp = sh.item[6];
+    } else {   // one-dimensional grid in (request, head, row group, chunk) order
         const int i = static_cast<int>(blockIdx.x);
         g.chunk = i % p.max_chunks;
-        g.kvh = (i / p.max_chunks) % p.Hkv;
-        g.b = i / (p.max_chunks * p.Hkv);
+        g.grp = (i / p.max_chunks) % p.tc_groups;
+        g.kvh = (i / (p.max_chunks * p.tc_groups)) % p.Hkv;
+        g.b = i / (p.max_chunks * p.tc_groups * p.Hkv);
         g.L = p.ctx_len[g.b];
         nn_loaded = p.n_nodes[g.b];
     }
     g.G = p.G;
-    g.R = p.R;
+    g.r0 = 256 * g.grp;
+    g.R = g.grp + 1 < p.tc_groups ? 256 : p.R - g.r0;
     g.bad = false;
     if (g.L < 0 || g.L > p.max_pages * p.page_size) { g.bad = true; g.L = 0; }
     const int nt_ctx = (g.L + kKeys - 1) / kKeys;
@@ -297,7 +308,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         if (g.chunk == 0) {
             if (tid == 0) report(p.dev_status, DDT_DEV_BAD_CTX);
             for (int x = tid; x < g.R * (kD / 8); x += kThreads) {
-                const int r = x / (kD / 8), c = x % (kD / 8);
+                const int r = g.r0 + x / (kD / 8), c = x % (kD / 8);
                 const int i = r / g.G, h = g.kvh * g.G + r % g.G;
                 *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD + c * 8) =
                     make_uint4(0, 0, 0, 0);
@@ -330,7 +341,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                 for (int h = 0; h < 2; ++h)
                     tma_load_4d(sQ + t * kQTileBytes + h * (kQTileBytes / 2), &maps.q,
                                 bar_addr(sh.q_full), 64 * h, 0, g.kvh,
-                                g.b * p.N + t * nodes_per_tile);
+                                g.b * p.N + g.r0 / g.G + t * nodes_per_tile);
         }
         for (int j = 0; j < g.n_tiles; ++j) {
             const int s = j % kStages;
@@ -494,7 +505,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         const int r = 128 * t + row_local;
         const bool active = t < g.n_main;
         const bool valid_row = active && r < g.R;
-        const int node = valid_row ? r / g.G : 0;
+        const int node = valid_row ? (g.r0 + r) / g.G : 0;
         const bool real = valid_row && node < g.nn;
         uint32_t visw[4] = {0u, 0u, 0u, 0u};
         if (real)
@@ -522,6 +533,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_addr(sh.q_tmem));   // one arrival per warp
+        } else if (t < n_main_all && lane == 0) {
+            mbar_arrive(bar_addr(sh.q_tmem));   // a tile this row group does not use
         }
         const float sc = p.scale_log2;            // > 0 on this path
         float m_ref = -INFINITY;                  // reference max, scaled log2 units
@@ -617,7 +630,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         if (active) {
             const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.o_final[t]), 0, abort));
             tc_fence_after();
-            const int i = node, h = g.kvh * g.G + (valid_row ? r % g.G : 0);
+            const int i = node, h = g.kvh * g.G + (valid_row ? (g.r0 + r) % g.G : 0);
             const bool good = done && ok;
             // Rows leave through a per-warp staging block in the (now idle) Q region of
             // shared memory, so that each store instruction writes whole rows.
@@ -646,7 +659,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                         const int rr = 8 * k + (lane >> 2), q4 = lane & 3;
                         const int rg = 128 * t + 32 * qw + rr;
                         if (rg < g.R) {
-                            const int ir = rg / g.G, hr = g.kvh * g.G + rg % g.G;
+                            const int ir = (g.r0 + rg) / g.G, hr = g.kvh * g.G + (g.r0 + rg) % g.G;
                             *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(g.b) * p.N + ir) * p.Hq + hr) * kD +
                                                       32 * c + 8 * q4) =
                                 *reinterpret_cast<const uint4*>(stage + rr * 20 + 4 * q4);
@@ -677,14 +690,23 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                         const int rr = 4 * k + (lane >> 3), q4 = lane & 7;
                         const int rg = 128 * t + 32 * qw + rr;
                         if (rg < g.R)
-                            *reinterpret_cast<float4*>(p.ws_o + (slot * p.R + rg) * kD + 32 * c + 4 * q4) =
+                            *reinterpret_cast<float4*>(p.ws_o + (slot * p.R + g.r0 + rg) * kD + 32 * c + 4 * q4) =
                                 *reinterpret_cast<const float4*>(fst + rr * 36 + 4 * q4);
                     }
                     __syncwarp();
                 }
                 if (valid_row)
-                    p.ws_ml[slot * p.R + r] = good ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.0f);
+                    p.ws_ml[slot * p.R + g.r0 + r] = good ? make_float2(m_ref, l_sum) : make_float2(-INFINITY, 0.0f);
             }
+        }
+    } else if (warp >= 12 && side_all && g.n_side == 0) {
+        // a row group without leftover rows in a launch whose last group has
+        // them: these warps still release every K/V stage the ring counts on
+        bool ok = true;
+        for (int j = 0; ok && j < g.n_tiles; ++j) {
+            const int s = j % kStages;
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.kv_full[s]), (j / kStages) & 1, abort));
+            if (ok && lane == 0) mbar_arrive(bar_addr(sh.kv_empty[s]));
         }
     } else if (warp >= 12 && g.n_side > 0) {
         // ---------------- leftover rows on mma.sync ----------------
@@ -696,7 +718,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         {
             const int sr = nrow;
             const bool ok = sr < g.n_side;
-            const int r = 256 + (ok ? sr : 0);
+            const int r = g.r0 + 256 + (ok ? sr : 0);
             const int i = r / g.G, h = g.kvh * g.G + r % g.G;
             const bf16_t* qrow = p.q + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD;
 #pragma unroll
@@ -711,7 +733,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int sr = crow0 + q;
-            node_r[q] = sr < g.n_side ? (256 + sr) / g.G : -1;
+            node_r[q] = sr < g.n_side ? (g.r0 + 256 + sr) / g.G : -1;
 #pragma unroll
             for (int w = 0; w < 4; ++w)
                 visr[q][w] = (node_r[q] >= 0 && node_r[q] < g.nn && w < p.W)
@@ -868,7 +890,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             }
         }
         if (sr < g.n_side) {
-            const int r = 256 + sr;
+            const int r = g.r0 + 256 + sr;   // the request's row
             const int i = r / g.G, h = g.kvh * g.G + r % g.G;
             const float lt = sh.side_l[0][sr] + sh.side_l[1][sr] + sh.side_l[2][sr] + sh.side_l[3][sr];
             const float mrun = sh.side_m[sr];
@@ -935,7 +957,7 @@ bool encode(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* ba
 // True when tree_verify_attn's sizes fit the tensor-core kernel.
 bool attn_tc_supported(const AttnParams& p) {
     if (p.Dh != kD || 128 % p.G != 0 || !(p.scale_log2 > 0.0f)) return false;
-    if (p.R > 256 + kMaxSide || p.n_groups != 1) return false;
+    if (p.tc_groups < 1 || p.R > 256 * (p.tc_groups - 1) + 256 + kMaxSide) return false;
     if (p.page_size < kKeys ? (kKeys % p.page_size) != 0 : (p.page_size % kKeys) != 0) return false;
     return true;
 }
@@ -974,7 +996,7 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.max_chunks) * p.Hkv * p.B;
+    const long long ctas = static_cast<long long>(p.max_chunks) * p.Hkv * p.tc_groups * p.B;
     if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     attn_tc_kernel<<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(p, maps);
     return cudaGetLastError();
