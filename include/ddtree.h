@@ -204,6 +204,10 @@ int ddtree_build(const float* topk_logp, const int32_t* topk_tok,
  * (their values may be anything, NaN included).
  * Supported: Dh in {64, 128}; 1 <= Hkv <= Hq, Hq % Hkv == 0; N <= 128;
  * page_size a multiple of 16 in [16, 1024]; ctx_len[b] <= max_pages * page_size.
+ * Kernels: Dh 128 with G = Hq / Hkv <= 128 and a page size that divides or is
+ * a multiple of 64 runs the tensor-core kernel (any number of rows N * G, in
+ * row groups); other supported shapes run a warp-MMA kernel, slower, with
+ * results within the same tolerance.
  * Device errors: DDT_DEV_BAD_PAGE (that page's slots are read as zeros),
  * DDT_DEV_BAD_CTX (the request's rows are zeros).
  */

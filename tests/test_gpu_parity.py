@@ -198,6 +198,12 @@ def test_attn_tiny_full():
     ([2500, 5], 16, 64, 4, 128, 32, 8, 8),          # G = 16, 528 rows: 256 + 256 + 16
     ([1200], 64, 32, 4, 128, 127, 4, 10),           # 1024 rows: four groups
     ([900, 4000], 32, 16, 4, 128, 99, 6, 9),        # 400 rows: 256 + 144 (a partial second tile)
+    # GQA groups that do not divide 128: tiles of whole nodes (126, 125, 120 rows)
+    ([2000, 300], 64, 28, 4, 128, 32, 8, 8),        # G = 7, 231 rows: 126 + 105
+    ([1500], 64, 28, 4, 128, 36, 6, 7),             # G = 7, 259 rows: 126 + 126 + 7 leftover
+    ([700], 32, 24, 8, 128, 64, 8, 9),              # G = 3, 195 rows
+    ([5000], 64, 96, 8, 128, 32, 8, 8),             # G = 12, 396 rows: 240 + 156
+    ([1100, 10], 64, 40, 8, 128, 52, 6, 7),         # G = 5, 265 rows: 250 + 15
 ])
 def test_attn_ragged_shapes(ctx, page_size, Hq, Hkv, Dh, budget, K, D):
     w = S.Workload(name="ragged", B=len(ctx), D=D, V=300, K=K, budget=budget, Hq=Hq, Hkv=Hkv,

@@ -224,9 +224,14 @@ int attn_call(const ddtree_bf16* q, const ddtree_bf16* k_tree, const ddtree_bf16
     p.tiles_per_chunk = pl.tiles_per_chunk; p.max_chunks = pl.max_chunks;
     // fewer merge rows than 32 warps per SM: occupancy cannot hide the loads
     p.merge_wide = static_cast<long long>(pl.R) * Hkv * B <= 32ll * plan_sms() ? 1 : 0;
-    // tensor-core path: groups of two 128-row tiles; up to 8 more rows ride in the
-    // last full group as leftover rows, a longer rest takes a group of its own
-    p.tc_groups = pl.R <= 256 + 8 ? 1 : pl.R / 256 + (pl.R % 256 > 8 ? 1 : 0);
+    // tensor-core path: groups of two tiles of rpt rows (the whole nodes that fit in
+    // 128 rows); up to 8 more rows ride in the last full group as leftover rows, a
+    // longer rest takes a group of its own
+    {
+        const int G = Hq / Hkv;
+        const int rpt = G <= 128 ? (128 / G) * G : 0;
+        p.tc_groups = rpt == 0 ? 0 : pl.R <= 2 * rpt + 8 ? 1 : pl.R / (2 * rpt) + (pl.R % (2 * rpt) > 8 ? 1 : 0);
+    }
     p.scale_log2 = scale * 1.4426950408889634f;
     p.stall_ns = stall_ns;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -6,12 +6,14 @@
 // loaded once and shared by all rows); "The Pivot Point", The Design
 // Constraint (load contexts once).
 //
-// One CTA owns every query row of one (request, KV head) and one chunk of its
+// One CTA owns one row group of one (request, KV head) and one chunk of its
 // context (a request's context is cut into chunks of equal length; with a
 // split context, warp 0 of each CTA first maps the block index to a work
-// item so that the longest chunks are dispatched first). Its R = N * G rows
-// (node-major: row r = node r / G, head r % G) are two 128-row tensor-core
-// tiles plus up to 8 leftover rows:
+// item so that the longest chunks are dispatched first). The R = N * G rows
+// (node-major: row r = node r / G, head r % G) fall in row groups of two
+// tensor-core tiles; a tile holds the whole nodes that fit in 128 rows (128
+// rows when G divides 128, else 128 - 128 % G), and the last group takes the
+// rest: two tiles plus up to 8 leftover rows, or fewer rows. A group's rows:
 //
 //   warp 0       TMA producer: Q once, then paged K/V tiles of 64 keys (one
 //                page box per half of the head dim, 128-byte swizzle) into a
@@ -102,6 +104,7 @@ struct Geometry {
     int b, kvh, chunk, L, nn, nchunks, t_begin, n_ctx, n_tree, n_tiles;
     int R, G, n_main, n_side;
     int grp, r0;              // row group and its first row (rows r0 .. r0 + R - 1 of the request's G * N)
+    int rpt;                  // rows of a tile: the whole nodes that fit in 128 lanes
     bool bad;
 };
 
@@ -210,6 +213,9 @@ DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* it
     }
 }
 
+// kWholeTile: G divides 128, so a tile's rows are all 128 lanes (a compile-time
+// constant in the row arithmetic); otherwise the whole nodes that fit.
+template <bool kWholeTile>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     extern __shared__ unsigned char smem_raw[];
@@ -226,8 +232,10 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     // softmax warps of n_main_all tiles (those of a tile a short row group does
     // not use arrive without work), and when the last row group has leftover
     // rows the leftover-row warps of every CTA take part in the K/V ring.
-    const int n_main_all = p.R > 128 ? 2 : 1;
-    const bool side_all = p.R - 256 * (p.tc_groups - 1) > 256;
+    const int n_main_all = p.R > (kWholeTile ? 128 : (128 / p.G) * p.G) ? 2 : 1;
+    // rows of a 128-lane tile: whole nodes only (a tile's Q box holds 128 / G nodes)
+    const int rpt = kWholeTile ? 128 : (128 / p.G) * p.G;
+    const bool side_all = p.R - 2 * rpt * (p.tc_groups - 1) > 2 * rpt;
     {
         const int n_main = n_main_all;
         const bool side = side_all;
@@ -287,8 +295,9 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         nn_loaded = p.n_nodes[g.b];
     }
     g.G = p.G;
-    g.r0 = 256 * g.grp;
-    g.R = g.grp + 1 < p.tc_groups ? 256 : p.R - g.r0;
+    g.rpt = rpt;
+    g.r0 = 2 * rpt * g.grp;
+    g.R = g.grp + 1 < p.tc_groups ? 2 * rpt : p.R - g.r0;
     g.bad = false;
     if (g.L < 0 || g.L > p.max_pages * p.page_size) { g.bad = true; g.L = 0; }
     const int nt_ctx = (g.L + kKeys - 1) / kKeys;
@@ -301,8 +310,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     g.n_ctx = static_cast<int>(static_cast<long long>(nt_ctx) * (g.chunk + 1) / g.nchunks) - g.t_begin;
     g.n_tree = (g.chunk == g.nchunks - 1) ? (p.N + kKeys - 1) / kKeys : 0;
     g.n_tiles = g.n_ctx + g.n_tree;
-    g.n_main = g.R > 128 ? 2 : 1;
-    g.n_side = max(0, g.R - 256);
+    g.n_main = g.R > rpt ? 2 : 1;
+    g.n_side = max(0, g.R - 2 * rpt);
 
     if (g.bad) {   // the request's rows are zeros
         if (g.chunk == 0) {
@@ -335,7 +344,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         for (int s = 0; s < kStages; ++s) last_issued[s] = -1;
         int pf_base = -1, pf_page = 0;
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar_addr(sh.q_full), g.n_main * kQTileBytes);
+            mbar_arrive_expect_tx(bar_addr(sh.q_full), g.n_main * (kQTileBytes / 128) * g.rpt);
             const int nodes_per_tile = 128 / g.G;
             for (int t = 0; t < g.n_main; ++t)
                 for (int h = 0; h < 2; ++h)
@@ -502,9 +511,9 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         const int t = (warp - 4) / 4;
         const int qw = warp & 3;
         const int row_local = 32 * qw + lane;
-        const int r = 128 * t + row_local;
+        const int r = g.rpt * t + row_local;
         const bool active = t < g.n_main;
-        const bool valid_row = active && r < g.R;
+        const bool valid_row = active && row_local < g.rpt && r < g.R;
         const int node = valid_row ? (g.r0 + r) / g.G : 0;
         const bool real = valid_row && node < g.nn;
         uint32_t visw[4] = {0u, 0u, 0u, 0u};
@@ -522,7 +531,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
                 uint32_t w[32];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    const uint4 v = q_ok ? *reinterpret_cast<const uint4*>(
+                    // rows past the tile's whole nodes hold no Q: zeros
+                    const uint4 v = (q_ok && row_local < g.rpt) ? *reinterpret_cast<const uint4*>(
                                                qrow + hh * (kQTileBytes / 2) + sw128_offset(row_local, c))
                                          : make_uint4(0, 0, 0, 0);
                     w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
@@ -657,8 +667,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {   // 8 rows x 64 bytes per instruction
                         const int rr = 8 * k + (lane >> 2), q4 = lane & 3;
-                        const int rg = 128 * t + 32 * qw + rr;
-                        if (rg < g.R) {
+                        const int rg = g.rpt * t + 32 * qw + rr;
+                        if (32 * qw + rr < g.rpt && rg < g.R) {
                             const int ir = (g.r0 + rg) / g.G, hr = g.kvh * g.G + (g.r0 + rg) % g.G;
                             *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(g.b) * p.N + ir) * p.Hq + hr) * kD +
                                                       32 * c + 8 * q4) =
@@ -688,8 +698,8 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {   // 4 rows x 128 bytes per instruction
                         const int rr = 4 * k + (lane >> 3), q4 = lane & 7;
-                        const int rg = 128 * t + 32 * qw + rr;
-                        if (rg < g.R)
+                        const int rg = g.rpt * t + 32 * qw + rr;
+                        if (32 * qw + rr < g.rpt && rg < g.R)
                             *reinterpret_cast<float4*>(p.ws_o + (slot * p.R + g.r0 + rg) * kD + 32 * c + 4 * q4) =
                                 *reinterpret_cast<const float4*>(fst + rr * 36 + 4 * q4);
                     }
@@ -718,7 +728,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         {
             const int sr = nrow;
             const bool ok = sr < g.n_side;
-            const int r = g.r0 + 256 + (ok ? sr : 0);
+            const int r = g.r0 + 2 * g.rpt + (ok ? sr : 0);
             const int i = r / g.G, h = g.kvh * g.G + r % g.G;
             const bf16_t* qrow = p.q + ((static_cast<size_t>(g.b) * p.N + i) * p.Hq + h) * kD;
 #pragma unroll
@@ -733,7 +743,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int sr = crow0 + q;
-            node_r[q] = sr < g.n_side ? (g.r0 + 256 + sr) / g.G : -1;
+            node_r[q] = sr < g.n_side ? (g.r0 + 2 * g.rpt + sr) / g.G : -1;
 #pragma unroll
             for (int w = 0; w < 4; ++w)
                 visr[q][w] = (node_r[q] >= 0 && node_r[q] < g.nn && w < p.W)
@@ -890,7 +900,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             }
         }
         if (sr < g.n_side) {
-            const int r = g.r0 + 256 + sr;   // the request's row
+            const int r = g.r0 + 2 * g.rpt + sr;   // the request's row
             const int i = r / g.G, h = g.kvh * g.G + r % g.G;
             const float lt = sh.side_l[0][sr] + sh.side_l[1][sr] + sh.side_l[2][sr] + sh.side_l[3][sr];
             const float mrun = sh.side_m[sr];
@@ -956,8 +966,9 @@ bool encode(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* m, const void* ba
 
 // True when tree_verify_attn's sizes fit the tensor-core kernel.
 bool attn_tc_supported(const AttnParams& p) {
-    if (p.Dh != kD || 128 % p.G != 0 || !(p.scale_log2 > 0.0f)) return false;
-    if (p.tc_groups < 1 || p.R > 256 * (p.tc_groups - 1) + 256 + kMaxSide) return false;
+    if (p.Dh != kD || p.G > 128 || !(p.scale_log2 > 0.0f)) return false;
+    const int rpt = (128 / p.G) * p.G;
+    if (p.tc_groups < 1 || p.R > 2 * rpt * p.tc_groups + kMaxSide) return false;
     if (p.page_size < kKeys ? (kKeys % p.page_size) != 0 : (p.page_size % kKeys) != 0) return false;
     return true;
 }
@@ -993,12 +1004,15 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t stream) {
         if (!encode(fn, &maps.kt, p.k_tree, 3, dims, str, box)) return cudaErrorInvalidValue;
         if (!encode(fn, &maps.vt, p.v_tree, 3, dims, str, box)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const bool whole = 128 % p.G == 0;
+    cudaError_t e = cudaFuncSetAttribute(whole ? attn_tc_kernel<true> : attn_tc_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.max_chunks) * p.Hkv * p.tc_groups * p.B;
     if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-    attn_tc_kernel<<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(p, maps);
+    if (whole) attn_tc_kernel<true><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(p, maps);
+    else attn_tc_kernel<false><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
