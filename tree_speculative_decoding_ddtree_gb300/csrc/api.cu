@@ -83,6 +83,13 @@ int plan_sms() {
     return v;
 }
 constexpr int kKeyTile = 64;
+// chunk-count model, in key-tile times of one SM (about 0.87 us for 264 rows of
+// Dh 128 on the tensor-core path): a work item's fixed cost (start, Q, first
+// tiles in flight, epilogue: about 9.6 us), the merge launch's fixed cost, and
+// the bytes all SMs move in one key-tile time (one 32 KB K/V tile each)
+constexpr long long kItemFixedTiles = 11;
+constexpr long long kMergeFixedTiles = 5;
+constexpr long long kTileBytesPerSm = 32768;
 
 struct AttnPlan {
     int R, rows_per_group, n_groups, tiles_per_chunk, max_chunks;
@@ -102,10 +109,39 @@ bool plan_attn(int B, int N, int Hq, int Hkv, int Dh, long long max_ctx, AttnPla
     pl->rows_per_group = static_cast<int>((per + 15) / 16 * 16);
     if (pl->rows_per_group > kMaxRowsPerCta) pl->rows_per_group = kMaxRowsPerCta;
     const long long tiles = (max_ctx + kKeyTile - 1) / kKeyTile;
-    const long long total = static_cast<long long>(B) * Hkv * pl->n_groups * (tiles > 0 ? tiles : 1);
-    const long long slots = static_cast<long long>(plan_sms()) * kPlanWaves;
+    const long long units = static_cast<long long>(B) * Hkv * pl->n_groups;
+    const long long total = units * (tiles > 0 ? tiles : 1);
+    const int sms = plan_sms();
+    const long long slots = static_cast<long long>(sms) * kPlanWaves;
     long long tpc = (total + slots - 1) / slots;
     if (tpc < 4) tpc = 4;
+    if (tiles > 0) {
+        // The wave target gives the fewest chunks per full-length context; from
+        // there up to four times as many, take the count whose work items of a
+        // batch of full-length contexts finish first: whole waves of equal items
+        // (each its tiles plus a fixed cost) plus the merge's partial traffic,
+        // all in key-tile times of one SM. Chunks are then as long as that count
+        // needs and no longer.
+        const long long nch0 = (tiles + tpc - 1) / tpc;
+        long long nch_hi = 4 * nch0;
+        if (nch_hi > tiles / 4) nch_hi = tiles / 4;
+        if (nch_hi < nch0) nch_hi = nch0;
+        long long best_n = nch0, best_cost = -1;
+        for (long long n = nch0; n <= nch_hi; ++n) {
+            const long long t = (tiles + n - 1) / n;
+            if ((tiles + t - 1) / t != n) continue;   // no chunk length gives exactly n chunks
+            const long long waves = (units * n + sms - 1) / sms;
+            long long cost = waves * (kItemFixedTiles + t);
+            if (n > 1) {
+                const long long part = 2 * units * n * (R / pl->n_groups) * Dh * 4;   // written, then read
+                cost += (part + static_cast<long long>(sms) * kTileBytesPerSm - 1) /
+                            (static_cast<long long>(sms) * kTileBytesPerSm) + kMergeFixedTiles;
+            }
+            if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_n = n; }
+        }
+        tpc = (tiles + best_n - 1) / best_n;
+        if (tpc < 4) tpc = 4;
+    }
     pl->tiles_per_chunk = static_cast<int>(tpc);
     pl->max_chunks = tiles > 0 ? static_cast<int>((tiles + tpc - 1) / tpc) : 1;
     const size_t rows = static_cast<size_t>(B) * Hkv * pl->max_chunks * R;
