@@ -30,7 +30,7 @@ struct BuildSmem {
     int n_parent[kMaxN];
     int n_depth[kMaxN];
     int n_rank[kMaxN];
-    int n_token[kMaxN];
+    int root_token;
     int n_first_child[kMaxN];
     int n_next_sibling[kMaxN];
 };
@@ -102,6 +102,13 @@ struct WarpHeap {
 
 // lp: the request's top-k log-probs, already widened to fp64 (exactly), so
 // the loop's only fp64 instructions are the two independent score adds per pop.
+// Every lane computes both new scores from the same shared-memory values (no
+// broadcast on the critical path); lane 0 alone records the node. The list
+// keeps only entries that can still be popped: an entry at place p needs p + 1
+// more pops to reach the front (inserts only move entries back), so with
+// budget - count pops left anything past that place never matters, and
+// SLOTS * 32 >= budget places suffice. An insert into a full list drops its
+// last entry.
 // A node's first child is its rank-0 child and the next sibling of a rank-r
 // node the rank-(r+1) node it pushed (a sibling is pushed only when the one
 // before it is added), so both links are known when a node is added.
@@ -124,21 +131,20 @@ DDT_DEVINL int build_pops(BuildSmem& s, const double* lp, const int32_t* tk, int
                   r = static_cast<int>((code >> 8) & 0xffu), p = static_cast<int>(code & 0xffu);
         ++count;
         const int i = count;
-        double cs = 0.0, ss = 0.0;
+        const double sc = key_score(bk);
+        const double cs = d < D ? sc + lp[d * K] : 0.0;                                // best child
+        const double ss = r + 1 < K ? s.n_score[p] + lp[(d - 1) * K + r + 1] : 0.0;    // next sibling
+        // the node's record (its token is looked up from depth and rank afterwards)
         if (lane == 0) {
-            const double sc = key_score(bk);
             s.n_score[i] = sc;
             s.n_parent[i] = p;
             s.n_depth[i] = d;
             s.n_rank[i] = r;
-            s.n_token[i] = tk[(d - 1) * K + r];
             if (r == 0) s.n_first_child[p] = i;
             else s.n_next_sibling[q] = i;
-            if (d < D) cs = sc + lp[d * K];                                 // best child
-            if (r + 1 < K) ss = s.n_score[p] + lp[(d - 1) * K + r + 1];      // next sibling
         }
-        const unsigned long long ck = __shfl_sync(0xffffffffu, score_key(cs), 0);
-        const unsigned long long sk = __shfl_sync(0xffffffffu, score_key(ss), 0);
+        const unsigned long long ck = score_key(cs);
+        const unsigned long long sk = score_key(ss);
         if (d < D) {   // the child is pushed before the sibling
             h.insert(ck, entry_code(d + 1, 0, 0, i), lane);
             ++live;
@@ -181,14 +187,14 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
         s.n_parent[0] = -1;
         s.n_depth[0] = 0;
         s.n_rank[0] = 0;
-        s.n_token[0] = root_tok[b];
+        s.root_token = root_tok[b];
     }
     for (int i = lane; i < N; i += 32) { s.n_first_child[i] = -1; s.n_next_sibling[i] = -1; }
     __syncwarp();
 
-    int count;
-    if (N <= 32) count = build_pops<1>(s, lp, tk, D, K, budget, lane);
-    else if (N <= 64) count = build_pops<2>(s, lp, tk, D, K, budget, lane);
+    int count;   // the list needs budget places (see build_pops)
+    if (budget <= 32) count = build_pops<1>(s, lp, tk, D, K, budget, lane);
+    else if (budget <= 64) count = build_pops<2>(s, lp, tk, D, K, budget, lane);
     else count = build_pops<4>(s, lp, tk, D, K, budget, lane);
     const int n = count + 1;
     __syncwarp();
@@ -202,7 +208,7 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
             for (int a = i; a >= 0; a = s.n_parent[a]) vw[a >> 5] |= 1u << (a & 31);
         parent[base + i] = real ? s.n_parent[i] : -1;
         depth[base + i] = real ? s.n_depth[i] : -1;
-        token[base + i] = real ? s.n_token[i] : -1;
+        token[base + i] = !real ? -1 : (i == 0 ? s.root_token : tk[(s.n_depth[i] - 1) * K + s.n_rank[i]]);
         rank[base + i] = real ? s.n_rank[i] : -1;
         pos[base + i] = real ? L + s.n_depth[i] : -1;
         score[base + i] = real ? s.n_score[i] : -INFINITY;
