@@ -47,6 +47,19 @@ int ddtree_testing_attn_stall(const ddtree_bf16* q, const ddtree_bf16* k_tree,
                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
                               void* stream, uint64_t stall_ns);
 
+/*
+ * ddtree_testing_gumbel - the Gumbel noise the temperature walks add to each
+ * token's scaled logit for the bonus draw ("The Architecture of Speculative
+ * Decoding", Section 3: the bonus comes from the residual distribution, drawn
+ * here as a Gumbel-max), for given Philox words.
+ *
+ * words (device, n uint32): Philox output words; U = ((w >> 8) + 0.5) 2^-24.
+ * out (device, n fp32): g = -log(-log U) as the walks compute it in fp32.
+ * Returns DDT_OK (n == 0: nothing runs), DDT_EINVAL for NULL pointers,
+ * DDT_ECUDA if the launch fails. Asynchronous on `stream`.
+ */
+int ddtree_testing_gumbel(const uint32_t* words, float* out, size_t n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -218,6 +218,14 @@ def test_sample_rejects_missing_rng_inputs_and_large_offset(lib):
     assert lib.ddtree_accept_sample(*walk_args(sample=True, offset=1 << 56)) == -1
 
 
+def test_gumbel_probe_rejects_null_before_any_cuda_call(lib):
+    fn = lib.ddtree_testing_gumbel
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert fn(None, None, 0, None) == 0    # nothing to do
+    assert fn(None, None, 4, None) == -1   # DDT_EINVAL
+
+
 def test_step_args_mirror_matches_the_c_struct(lib):
     import tree_speculative_decoding_ddtree_gb300 as dd
     assert lib.ddtree_step_args_size() == ctypes.sizeof(dd.StepArgs)

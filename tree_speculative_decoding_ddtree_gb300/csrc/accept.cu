@@ -258,6 +258,12 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         unsigned long long best = 0ull;
         Gap2 gap{-INFINITY, -INFINITY};
         const int g0 = vec4 ? sl.g0 : (sl.g0 >> 2), g1 = vec4 ? sl.g1 : ((sl.g1 + 3) >> 2);
+        // does any child's token fall in this thread's groups of four (x = g0 + tid + 512 i)?
+        bool kid_here = false;
+        for (int k = 0; k < nk; ++k) {
+            const int xk = s_kid_tok[k] >> 2;
+            kid_here |= xk >= g0 && xk < g1 && (xk - g0 - static_cast<int>(threadIdx.x)) % kWalkThreads == 0;
+        }
 #pragma unroll 2
         for (int x = g0 + static_cast<int>(threadIdx.x); x < g1; x += kWalkThreads) {
             const uint4 w = philox4x32_10(make_uint4(1u | off_hi8, static_cast<uint32_t>(u),
@@ -276,10 +282,12 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
                 const int v = 4 * x + e;
                 // element slices: this CTA owns [g0, g1) of the elements only
                 if (v >= V || (!vec4 && (v < sl.g0 || v >= sl.g1))) continue;
-                bool kid = false;
-                for (int k = 0; k < nk; ++k) kid |= (s_kid_tok[k] == v);
-                if (kid) continue;
-                const float g = -logf(neg_log_uniform(ws[e]));
+                if (kid_here) {   // only threads holding a child's token look for it
+                    bool kid = false;
+                    for (int k = 0; k < nk; ++k) kid |= (s_kid_tok[k] == v);
+                    if (kid) continue;
+                }
+                const float g = gumbel_noise(ws[e]);
                 const float sc = f[e] * inv_t + g;
                 const unsigned long long pk = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
                 best = best > pk ? best : pk;
@@ -333,6 +341,19 @@ cudaError_t launch_accept_sample(const float* logits, int V, const int32_t* toke
     accept_sample_kernel<<<B * kCluster, kWalkThreads, 0, stream>>>(logits, V, vec4, token, first_child,
                                                                     next_sibling, n_nodes, N, D, temperature,
                                                                     seed, offset, o, dev_status);
+    return cudaGetLastError();
+}
+
+// gumbel_noise of every word (the testing entry point's exhaustive check)
+__global__ void gumbel_probe_kernel(const uint32_t* __restrict__ words, float* __restrict__ out, size_t n) {
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        out[i] = gumbel_noise(words[i]);
+}
+
+cudaError_t launch_gumbel_probe(const uint32_t* words, float* out, size_t n, cudaStream_t stream) {
+    const size_t blocks = (n + 255) / 256;
+    gumbel_probe_kernel<<<static_cast<unsigned>(blocks < 4096 ? blocks : 4096), 256, 0, stream>>>(words, out, n);
     return cudaGetLastError();
 }
 

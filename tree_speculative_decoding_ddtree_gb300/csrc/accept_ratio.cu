@@ -354,7 +354,7 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                 } else {
                     sc = (f[e] - Mq) * inv_t;   // log q up to a constant
                 }
-                sc += -logf(neg_log_uniform(ws[e]));
+                sc += gumbel_noise(ws[e]);
                 const unsigned long long pk = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
                 best = best > pk ? best : pk;
                 if (want_gap) gap2_add(gap, sc);

@@ -26,6 +26,7 @@ cudaError_t launch_accept_both(const float*, int, const int32_t*, const int32_t*
                                const int32_t*, int, int, int, const float*, const uint64_t*, uint64_t,
                                const WalkOut&, const WalkOut&, int32_t*, cudaStream_t);
 cudaError_t launch_draft_topk(const float*, int, int, int, int, float*, int32_t*, cudaStream_t);
+cudaError_t launch_gumbel_probe(const uint32_t*, float*, size_t, cudaStream_t);
 cudaError_t launch_accept_ratio(const float*, const float*, int, const int32_t*, const int32_t*,
                                 const int32_t*, const int32_t*, int, int, int, const float*,
                                 const uint64_t*, uint64_t, int32_t*, int32_t*, int32_t*, int32_t*,
@@ -310,6 +311,14 @@ int ddtree_testing_attn_stall(const ddtree_bf16* q, const ddtree_bf16* k_tree,
     return attn_call(q, k_tree, v_tree, k_cache, v_cache, num_pages, page_size, page_table, max_pages,
                      ctx_len, vis, n_nodes, B, N, Hq, Hkv, Dh, scale, out, lse, workspace,
                      workspace_bytes, dev_status, stream, stall_ns);
+}
+
+int ddtree_testing_gumbel(const uint32_t* words, float* out, size_t n, void* stream) {
+    TraceRange trace("ddtree_testing_gumbel");
+    if (n == 0) return DDT_OK;
+    if (!words || !out) return DDT_EINVAL;
+    const cudaError_t e = launch_gumbel_probe(words, out, n, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DDT_OK : cuda_fail(e);
 }
 
 static int check_walk_args(const float* logits, int V, const int32_t* token,

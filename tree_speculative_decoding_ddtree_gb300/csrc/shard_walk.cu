@@ -258,7 +258,7 @@ shard_bonus_kernel(const float* __restrict__ logits, int Vs, int v0, const int32
         const uint4 w = philox4x32_10(make_uint4(1u | off_hi8, static_cast<uint32_t>(u), static_cast<uint32_t>(v >> 2),
                                                  off_lo), k0, k1);
         const uint32_t word = (v & 3) == 0 ? w.x : (v & 3) == 1 ? w.y : (v & 3) == 2 ? w.z : w.w;
-        const float sc = __ldg(row + i) * inv_t + -logf(neg_log_uniform(word));
+        const float sc = __ldg(row + i) * inv_t + gumbel_noise(word);
         const unsigned long long p = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
         best = best > p ? best : p;
     }
