@@ -63,6 +63,7 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
         for (int k = threadIdx.x; k <= D; k += kWalkThreads) {
             gtoks[k] = -1; gnodes[k] = -1; stoks[k] = -1; snodes[k] = -1;
         }
+    if (threadIdx.x == 0) prefetch_slice_l2(logits + tb * static_cast<size_t>(V), vec4, sl);
     stage_tree(tr, token, first_child, next_sibling, tb, N);
     const int nn_read = n_nodes[b];
     int nn = nn_read;

@@ -121,6 +121,7 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
     int32_t* nodes = o.out_nodes + static_cast<size_t>(b) * (D + 1);
     if (writer)
         for (int k = threadIdx.x; k <= D; k += kWalkThreads) { toks[k] = -1; nodes[k] = -1; }
+    if (threadIdx.x == 0) prefetch_slice_l2(logits + tb * static_cast<size_t>(V), vec4, sl);
     stage_tree(tr, token, first_child, next_sibling, tb, N);
     const int nn_read = n_nodes[b];
     int nn = nn_read;

@@ -132,6 +132,20 @@ DDT_DEVINL Slice row_slice(int V, bool vec4, uint32_t rank) {
     return s;
 }
 
+// Ask L2 for this CTA's slice of the root's logits row, which every walk reads
+// first, while the tree is staged (a hint: nothing waits for it). The range is
+// trimmed to 16-byte boundaries inside the slice, as the bulk prefetch needs.
+DDT_DEVINL void prefetch_slice_l2(const float* row, bool vec4, Slice sl) {
+    const uintptr_t unit = vec4 ? 16 : 4;
+    const uintptr_t lo = (reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(sl.g0) * unit + 15) &
+                         ~static_cast<uintptr_t>(15);
+    const uintptr_t hi = (reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(sl.g1) * unit) &
+                         ~static_cast<uintptr_t>(15);
+    if (hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n"
+                     :: "l"(lo), "r"(static_cast<uint32_t>(hi - lo)) : "memory");
+}
+
 // argmax of this CTA's slice (largest value, lowest index, NaN lowest), packed
 DDT_DEVINL unsigned long long slice_argmax(const float* __restrict__ row, bool vec4, Slice sl,
                                            unsigned long long* scratch) {
