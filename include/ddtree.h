@@ -287,6 +287,8 @@ int ddtree_accept_greedy(const float* logits, int V, const int32_t* token,
  * (purpose | (offset >> 32) << 8, node, index, offset lo32): purpose 0 =
  * child test (index = child slot, word 0), purpose 1 = Gumbel noise for vocab
  * entry v (index = v >> 2, word v & 3); uniform = ((w >> 8) + 0.5) * 2^-24.
+ * The noise g = -log(-log U) is formed in fp32 within 2e-6 of its exact value
+ * for every uniform (ddtree_testing_gumbel in ddtree_testing.h returns it).
  * Outputs: as ddtree_accept_greedy (walk_stats column 3 counts the child
  * tests that rejected), plus
  *   margin_stats  fp32 [B] (nullable): the smallest decision margin on the
