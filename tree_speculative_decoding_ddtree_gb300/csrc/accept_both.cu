@@ -45,7 +45,6 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
     __shared__ float s_kid_logit[kMaxKids];
     __shared__ float s_q[kMaxKids];
     __shared__ double s_u[kMaxKids];
-    __shared__ float s_m, s_z;
     __shared__ int s_nkids;
     __shared__ int s_gnext, s_snext;
     __shared__ int s_glen, s_grej, s_slen, s_srej;
@@ -122,8 +121,14 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
         __syncthreads();
         const int nk = s_nkids;
         if (s_walk && threadIdx.x < nk) {
-            const int x = s_kid_tok[threadIdx.x];
-            s_kid_logit[threadIdx.x] = (x >= 0 && x < V) ? __ldg(srow + x) : 0.0f;
+            // child j's logit and its uniform (the uniform needs no statistics of
+            // the row, so it is drawn before the round's cluster barrier)
+            const int j = threadIdx.x;
+            const int x = s_kid_tok[j];
+            s_kid_logit[j] = (x >= 0 && x < V) ? __ldg(srow + x) : 0.0f;
+            const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(us),
+                                                     static_cast<uint32_t>(j), off_lo), k0, k1);
+            s_u[j] = uniform_exact(w.x);
         }
         // This round's row passes, in one loop so that both rows' loads are in
         // flight together (one load when both walks stand on the same node): the
@@ -282,29 +287,22 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
             }
             s_gnext = match;
         }
-        if (s_walk) {
-            if (threadIdx.x < 32) {
-                // the same partials merged by the same shuffle tree in every CTA
-                const SMaxSum acc = sms_cluster(&part_ms[par]);
-                if (threadIdx.x == 0) {
-                    s_m = acc.m;
-                    s_z = acc.z;
-                }
-            }
-            __syncthreads();
-            // child j: q(x_j) and its uniform, one thread each
+        if (s_walk && threadIdx.x < 32) {
+            // warp 0 alone: the same partials merged by the same shuffle tree in
+            // every CTA, lane 0's result on every lane, q(x_j) of child j on lane j
+            // (at most 32 children), then the decision on lane 0
+            SMaxSum acc = sms_cluster(&part_ms[par]);
+            acc.m = __shfl_sync(0xffffffffu, acc.m, 0);
+            acc.z = __shfl_sync(0xffffffffu, acc.z, 0);
             if (threadIdx.x < nk) {
                 const int j = threadIdx.x;
                 const int x = s_kid_tok[j];
                 float q = 0.0f;
-                if (x >= 0 && x < V) q = ex2_approx(fmaf(s_kid_logit[j], s2, -s_m)) / s_z;
+                if (x >= 0 && x < V) q = ex2_approx(fmaf(s_kid_logit[j], s2, -acc.m)) / acc.z;
                 else if (writer) report(dev_status, DDT_DEV_BAD_TOKEN);
-                const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(us),
-                                                         static_cast<uint32_t>(j), off_lo), k0, k1);
                 s_q[j] = q;
-                s_u[j] = uniform_exact(w.x);
             }
-            __syncthreads();
+            __syncwarp();
             // children in rank order: accept child j when u_j * R < q(x_j)
             if (threadIdx.x == 0) {
                 int match = -1;
