@@ -118,7 +118,6 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
     __shared__ float s_kid_logit[kMaxKids];
     __shared__ float s_q[kMaxKids];
     __shared__ double s_u[kMaxKids];
-    __shared__ float s_m, s_z;
     __shared__ int s_nkids;
     __shared__ int s_next;
     __shared__ int s_len;
@@ -185,10 +184,15 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         }
         __syncthreads();
         const int nk = s_nkids;
-        // the children's logits are fetched while the slice streams
+        // the children's logits are fetched while the slice streams, and their
+        // uniforms drawn (they need no statistics of the row)
         if (threadIdx.x < nk) {
-            const int x = s_kid_tok[threadIdx.x];
-            s_kid_logit[threadIdx.x] = (x >= 0 && x < V) ? __ldg(row + x) : 0.0f;
+            const int j = threadIdx.x;
+            const int x = s_kid_tok[j];
+            s_kid_logit[j] = (x >= 0 && x < V) ? __ldg(row + x) : 0.0f;
+            const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(u),
+                                                     static_cast<uint32_t>(j), off_lo), k0, k1);
+            s_u[j] = uniform_exact(w.x);
         }
         // this CTA's slice: softmax statistics of logits / T in the exp2 domain
         SMaxSum ms{-INFINITY, 0.0f};
@@ -205,27 +209,22 @@ accept_sample_kernel(const float* __restrict__ logits, int V, bool vec4,
         if (threadIdx.x == 0) part_ms[level & 1] = make_float2(ms.m, ms.z);
         cluster_barrier();
         if (threadIdx.x < 32) {
-            // the same partials merged by the same shuffle tree in every CTA
-            const SMaxSum acc = sms_cluster(&part_ms[level & 1]);
-            if (threadIdx.x == 0) {
-                s_m = acc.m;
-                s_z = acc.z;
+            // warp 0 alone: the same partials merged by the same shuffle tree in
+            // every CTA, lane 0's result on every lane, q(x_j) of child j on lane j
+            // (at most 32 children), then the decision on lane 0
+            SMaxSum acc = sms_cluster(&part_ms[level & 1]);
+            acc.m = __shfl_sync(0xffffffffu, acc.m, 0);
+            acc.z = __shfl_sync(0xffffffffu, acc.z, 0);
+            if (threadIdx.x < nk) {
+                const int j = threadIdx.x;
+                const int x = s_kid_tok[j];
+                float q = 0.0f;
+                if (x >= 0 && x < V) q = ex2_approx(fmaf(s_kid_logit[j], s2, -acc.m)) / acc.z;
+                else if (writer) report(dev_status, DDT_DEV_BAD_TOKEN);
+                s_q[j] = q;
             }
+            __syncwarp();
         }
-        __syncthreads();
-        // child j: q(x_j) and its uniform, one thread each
-        if (threadIdx.x < nk) {
-            const int j = threadIdx.x;
-            const int x = s_kid_tok[j];
-            float q = 0.0f;
-            if (x >= 0 && x < V) q = ex2_approx(fmaf(s_kid_logit[j], s2, -s_m)) / s_z;
-            else if (writer) report(dev_status, DDT_DEV_BAD_TOKEN);
-            const uint4 w = philox4x32_10(make_uint4(0u | off_hi8, static_cast<uint32_t>(u),
-                                                     static_cast<uint32_t>(j), off_lo), k0, k1);
-            s_q[j] = q;
-            s_u[j] = uniform_exact(w.x);
-        }
-        __syncthreads();
         // children in rank order: accept child j when u_j * R < q(x_j)
         if (threadIdx.x == 0) {
             int match = -1;
