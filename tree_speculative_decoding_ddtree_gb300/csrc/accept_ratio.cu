@@ -15,7 +15,8 @@
 // U_j * p(x) < r(x). The bonus is the Gumbel-max of log max(q - c p, 0); if
 // the residual has no mass left the bonus is drawn from q.
 //
-// Precision: q and p are fp32 (expf over the row, fp32 sums); c and R are
+// Precision: q and p are fp32 (softmax statistics in the exp2 domain, each
+// power one ex2.approx of a fused multiply-add, fp32 sums); c and R are
 // fp64 scalars (R summed in fp64 across the threads' fp32 partials), and
 // every residual q - c p is formed with one fused multiply-add on the high
 // part of c (the low part's product subtracted after), so the subtraction
@@ -49,38 +50,6 @@ DDT_DEVINL float block_sum_f(float v, float* scratch) {
     }
     __syncthreads();
     return scratch[0];
-}
-
-// block-wide (max, sum) merge of one MaxSum per thread; thread 0 gets the result
-DDT_DEVINL MaxSum block_ms(MaxSum ms, float inv_t, float* sm, float* sz) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
-        ms = merge_ms(ms, other, inv_t);
-    }
-    __syncthreads();
-    if (lane == 0) { sm[warp] = ms.m; sz[warp] = ms.z; }
-    __syncthreads();
-    if (warp == 0) {
-        ms.m = lane < kWalkThreads / 32 ? sm[lane] : -INFINITY;
-        ms.z = lane < kWalkThreads / 32 ? sz[lane] : 0.0f;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            MaxSum other{__shfl_xor_sync(0xffffffffu, ms.m, off), __shfl_xor_sync(0xffffffffu, ms.z, off)};
-            ms = merge_ms(ms, other, inv_t);
-        }
-    }
-    return ms;
-}
-
-DDT_DEVINL void ms_add(MaxSum& ms, float x, float inv_t) {
-    if (x > ms.m) {
-        ms.z = ms.z * expf((ms.m - x) * inv_t) + 1.0f;
-        ms.m = x;
-    } else {
-        ms.z += expf((x - ms.m) * inv_t);
-    }
 }
 
 }  // namespace
@@ -142,6 +111,7 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
         return;
     }
     const float inv_t = 1.0f / T;
+    const float s2 = inv_t * 1.4426950408889634f;   // log2(e) / T: the statistics' exp2 units
     const uint64_t sd = seed[b];
     const uint32_t k0 = static_cast<uint32_t>(sd), k1 = static_cast<uint32_t>(sd >> 32);
     const uint32_t off_lo = static_cast<uint32_t>(offset);
@@ -188,39 +158,36 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                                                      static_cast<uint32_t>(j), off_lo), k0, k1);
             s_u[j] = uniform_exact(w.x);
         }
-        // pass 1: (max, sum) of the target row and, with children, of the draft row
-        MaxSum mq{-INFINITY, 0.0f}, mp{-INFINITY, 0.0f};
+        // pass 1: softmax statistics (exp2 domain) of the target row and, with
+        // children, of the draft row
+        SMaxSum mq{-INFINITY, 0.0f}, mp{-INFINITY, 0.0f};
         if (vec4) {
             const float4* r4 = reinterpret_cast<const float4*>(row);
             const float4* d4 = reinterpret_cast<const float4*>(drow);
 #pragma unroll 2
             for (int x = sl.g0 + static_cast<int>(threadIdx.x); x < sl.g1; x += kWalkThreads) {
-                const float4 f = __ldg(r4 + x);
-                ms_add(mq, f.x, inv_t); ms_add(mq, f.y, inv_t); ms_add(mq, f.z, inv_t); ms_add(mq, f.w, inv_t);
-                if (nk > 0) {
-                    const float4 g = __ldg(d4 + x);
-                    ms_add(mp, g.x, inv_t); ms_add(mp, g.y, inv_t); ms_add(mp, g.z, inv_t); ms_add(mp, g.w, inv_t);
-                }
+                sms_add4(mq, __ldg(r4 + x), s2);
+                if (nk > 0) sms_add4(mp, __ldg(d4 + x), s2);
             }
         } else {
             for (int v = sl.g0 + static_cast<int>(threadIdx.x); v < sl.g1; v += kWalkThreads) {
-                ms_add(mq, __ldg(row + v), inv_t);
-                if (nk > 0) ms_add(mp, __ldg(drow + v), inv_t);
+                sms_add1(mq, __ldg(row + v), s2);
+                if (nk > 0) sms_add1(mp, __ldg(drow + v), s2);
             }
         }
-        mq = block_ms(mq, inv_t, scratch_a, scratch_b);
-        mp = block_ms(mp, inv_t, scratch_a, scratch_b);
+        mq = sms_block(mq, scratch_a, scratch_b);
+        mp = sms_block(mp, scratch_a, scratch_b);
         if (threadIdx.x == 0) part_s[round & 1] = make_float4(mq.m, mq.z, mp.m, mp.z);
         cluster_barrier();
         if (threadIdx.x == 0) {   // the same partials merged in the same order in every CTA
-            MaxSum aq{-INFINITY, 0.0f}, ap{-INFINITY, 0.0f};
+            SMaxSum aq{-INFINITY, 0.0f}, ap{-INFINITY, 0.0f};
 #pragma unroll
             for (int r = 0; r < kCluster; ++r) {
                 const uint32_t a = cluster_addr(&part_s[round & 1], r);
                 const float2 q2 = ld_cluster_f32x2(a);
                 const float2 p2 = ld_cluster_f32x2(a + 8);
-                aq = merge_ms(aq, MaxSum{q2.x, q2.y}, inv_t);
-                ap = merge_ms(ap, MaxSum{p2.x, p2.y}, inv_t);
+                aq = sms_merge(aq, SMaxSum{q2.x, q2.y});
+                ap = sms_merge(ap, SMaxSum{p2.x, p2.y});
             }
             s_mq = aq.m; s_zq = aq.z; s_mp = ap.m; s_zp = ap.z;
             s_c = 0.0;
@@ -236,7 +203,7 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
         auto resid = [&](float qv, float pv) { return fmaxf(fmaf(-c_hi, pv, qv) - c_lo * pv, 0.0f); };
         // the residual of vocabulary entry v from its target and draft logits
         auto qp = [&](float l, float d) {
-            return resid(expf((l - Mq) * inv_t) * rZq, expf((d - Mp) * inv_t) * rZp);
+            return resid(ex2_approx(fmaf(l, s2, -Mq)) * rZq, ex2_approx(fmaf(d, s2, -Mp)) * rZp);
         };
         int match = -1;
         for (int j = 0; j < nk; ++j) {
@@ -247,8 +214,8 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                     if (writer) report(dev_status, DDT_DEV_BAD_TOKEN);
                     st = kSkip;
                 } else {
-                    const float qx = expf((s_kid_l[j] - Mq) * inv_t) * rZq;
-                    const float px = expf((s_kid_d[j] - Mp) * inv_t) * rZp;
+                    const float qx = ex2_approx(fmaf(s_kid_l[j], s2, -Mq)) * rZq;
+                    const float px = ex2_approx(fmaf(s_kid_d[j], s2, -Mp)) * rZp;
                     const double R = s_R;
                     const float ru = resid(qx, px);   // R r(x): the test U p(x) < r(x) without a divide
                     if (o.margin && px > 0.0f)        // fp32 is enough for the report
@@ -353,7 +320,7 @@ accept_ratio_kernel(const float* __restrict__ logits, const float* __restrict__ 
                     if (!(r > 0.0f)) continue;
                     sc = logf(r);
                 } else {
-                    sc = (f[e] - Mq) * inv_t;   // log q up to a constant
+                    sc = f[e] * inv_t;   // log q up to a constant (as the renormalising walk's bonus)
                 }
                 sc += gumbel_noise(ws[e]);
                 const unsigned long long pk = argmax_pack(float_order_key(sc), static_cast<uint32_t>(v));
