@@ -155,6 +155,54 @@ def test_workspace_size(lib):
     assert 0 < small <= big
 
 
+def _planned_workspace(B, N, Hq, Hkv, Dh, max_ctx, sms=152):
+    """The split-KV planner's workspace, restated: a three-wave target gives the
+    fewest chunks per full-length context; from there up to four times as many,
+    the count whose equal work items (tiles + 11 tiles of fixed cost, in whole
+    waves of the SMs) plus the merge's partial traffic (written and read, in
+    32 KB per SM per tile time, + 5 tiles) finish first; then the shortest
+    chunk length for that count."""
+    R = N * (Hq // Hkv)
+    groups = -(-R // 288)
+    tiles = -(-max_ctx // 64)
+    units = B * Hkv * groups
+    tpc = max(4, -(-units * max(tiles, 1) // (sms * 3)))
+    if tiles > 0:
+        nch0 = -(-tiles // tpc)
+        hi = max(nch0, min(4 * nch0, tiles // 4))
+        best = None
+        for n in range(nch0, hi + 1):
+            t = -(-tiles // n)
+            if -(-tiles // t) != n:
+                continue
+            cost = -(-units * n // sms) * (11 + t)
+            if n > 1:
+                cost += -(-(2 * units * n * (R // groups) * Dh * 4) // (sms * 32768)) + 5
+            if best is None or cost < best[0]:
+                best = (cost, n)
+        tpc = max(4, -(-tiles // best[1]))
+    chunks = -(-tiles // tpc) if tiles > 0 else 1
+    if chunks <= 1:
+        return 0
+    rows = B * Hkv * chunks * R
+    return -(-(rows * Dh * 4) // 256) * 256 + -(-(rows * 8) // 256) * 256
+
+
+@pytest.mark.parametrize("B,N,Hq,Hkv,Dh,max_ctx", [
+    (16, 33, 64, 8, 128, 16384),   # the bench batch: four chunks of 64 tiles
+    (64, 65, 32, 8, 128, 32768),   # the deep batch: two chunks of 256 tiles
+    (32, 33, 64, 8, 128, 8192),
+    (1, 33, 64, 8, 128, 4096),     # one request: the 4-tile floor
+    (3, 17, 16, 2, 64, 100000),
+    (8, 128, 48, 8, 128, 65536),   # several row groups
+    (40, 9, 8, 8, 128, 2048),
+])
+def test_workspace_size_follows_the_chunk_model(lib, B, N, Hq, Hkv, Dh, max_ctx):
+    # on a host without a usable device the planner sizes for 152 SMs, as here
+    assert lib.tree_verify_attn_workspace_size(B, N, Hq, Hkv, Dh, max_ctx) == \
+        _planned_workspace(B, N, Hq, Hkv, Dh, max_ctx)
+
+
 def walk_args(sample=False, **kw):
     a = dict(logits=FAKE, V=100, token=FAKE, fc=FAKE, ns=FAKE, nn=FAKE, B=2, N=33, D=8,
              acc=FAKE, toks=FAKE, nodes=FAKE, bonus=FAKE, margin=0, stats=0, status=0, stream=0,
