@@ -208,6 +208,12 @@ int ddtree_build(const float* topk_logp, const int32_t* topk_tok,
  * a multiple of 64 runs the tensor-core kernel (any number of rows N * G, in
  * row groups); other supported shapes run a warp-MMA kernel, slower, with
  * results within the same tolerance.
+ * Overlap with ddtree_build: the tensor-core kernel is launched as a
+ * programmatic dependent of the work before it on the stream. Directly after
+ * ddtree_build it starts while the build finishes (loading Q, the tree K/V
+ * and the paged context, which the build does not write) and reads n_nodes
+ * and vis only once the build's grid has completed; after any other work it
+ * starts when that work has completed, as an ordinary launch.
  * Device errors: DDT_DEV_BAD_PAGE (that page's slots are read as zeros),
  * DDT_DEV_BAD_CTX (the request's rows are zeros).
  */

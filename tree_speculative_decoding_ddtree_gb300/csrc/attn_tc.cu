@@ -40,6 +40,13 @@
 // other tile's softmax runs.
 // Every wait is bounded; a timeout sets DDT_DEV_TIMEOUT, drains the copies
 // and MMAs already issued, frees TMEM and returns.
+//
+// The kernel is a programmatic dependent of the build (which signals its
+// dependents as it starts): the work-item lookup reads only ctx_len, the
+// producer streams Q and the context at once, and the tree (n_nodes, the
+// masks) is read after griddepcontrol.wait, by the softmax warps once their Q
+// is in TMEM, by the leftover-row warps, and by the producer before its first
+// tree tile.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -97,7 +104,7 @@ struct TcShared {
     float side_m[kMaxSide];
     int map_cnt[kLptMaxB];    // work-item counts in rank order (the CTA's item lookup)
     int map_off[kLptMaxB];    // their exclusive prefix sums
-    int item[7];              // this CTA's (request, KV head, chunk, found, ctx_len, n_nodes, row group)
+    int item[7];              // this CTA's (request, KV head, chunk, found, ctx_len, unused, row group)
 };
 
 struct Geometry {
@@ -142,12 +149,11 @@ DDT_DEVINL uint32_t bar_addr(const uint64_t& b) { return smem_u32(&b); }
 // first and the short ones fill the tail (longest processing time first).
 DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* item) {
     const int lane = threadIdx.x & 31;
-    int key[2], nch[2], rnk[2], Lq[2], nnq[2];
+    int key[2], nch[2], rnk[2], Lq[2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {   // the loads of both slots first, then the arithmetic
+    for (int q = 0; q < 2; ++q) {
         const int b = lane + 32 * q;
         Lq[q] = b < p.B ? p.ctx_len[b] : 0;
-        nnq[q] = b < p.B ? p.n_nodes[b] : 0;
     }
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -205,7 +211,6 @@ DDT_DEVINL void lpt_item(const AttnParams& p, int i, int* cnt, int* off, int* it
             item[2] = local % nch[hit];
             item[3] = 1;
             item[4] = Lq[hit];
-            item[5] = nnq[hit];
             item[6] = (local / nch[hit]) % p.tc_groups;
         }
     } else if (lane == 0) {
@@ -276,14 +281,12 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     };
 
     Geometry g;
-    int nn_loaded;
     if (lpt) {   // one-dimensional grid, longest chunks first
         if (!sh.item[3]) { leave(); return; }
         g.b = sh.item[0];
         g.kvh = sh.item[1];
         g.chunk = sh.item[2];
         g.L = sh.item[4];
-        nn_loaded = sh.item[5];
         g.grp = sh.item[6];
     } else {   // one-dimensional grid in (request, head, row group, chunk) order
         const int i = static_cast<int>(blockIdx.x);
@@ -292,7 +295,6 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         g.kvh = (i / (p.max_chunks * p.tc_groups)) % p.Hkv;
         g.b = i / (p.max_chunks * p.tc_groups * p.Hkv);
         g.L = p.ctx_len[g.b];
-        nn_loaded = p.n_nodes[g.b];
     }
     g.G = p.G;
     g.rpt = rpt;
@@ -303,8 +305,21 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     const int nt_ctx = (g.L + kKeys - 1) / kKeys;
     g.nchunks = nt_ctx > 0 ? (nt_ctx + p.tiles_per_chunk - 1) / p.tiles_per_chunk : 1;
     if (g.chunk >= g.nchunks) { leave(); return; }
-    g.nn = nn_loaded;
-    if (g.nn < 0 || g.nn > p.N) { g.bad = true; g.nn = 0; }
+    // The tree (n_nodes, the masks) comes from the build, which may still be
+    // running (this kernel is its programmatic dependent): the roles that need
+    // it wait for the build's grid first (see read_tree). Everything before
+    // uses only the call's inputs.
+    g.nn = 0;
+    auto read_tree = [&]() {
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        const int nn = p.n_nodes[g.b];
+        if (nn < 0 || nn > p.N) {   // a malformed tree: no real rows (outputs zero, lse -inf)
+            if (lane == 0) report(p.dev_status, DDT_DEV_BAD_CTX);
+            g.nn = 0;
+        } else {
+            g.nn = nn;
+        }
+    };
     // the request's tiles in nchunks chunks of equal length (within one tile)
     g.t_begin = static_cast<int>(static_cast<long long>(nt_ctx) * g.chunk / g.nchunks);
     g.n_ctx = static_cast<int>(static_cast<long long>(nt_ctx) * (g.chunk + 1) / g.nchunks) - g.t_begin;
@@ -357,6 +372,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
             if (j >= kStages &&
                 !__all_sync(0xffffffffu, mbar_wait_bounded(bar_addr(sh.kv_empty[s]), ((j / kStages) - 1) & 1, abort)))
                 break;
+            if (j == g.n_ctx) read_tree();   // the tree tiles' valid rows need n_nodes
             const TileInfo ti = tile_info(g, j);
             const uint32_t kdst = sStage + s * kStageBytes;
             const uint32_t vdst = kdst + 2 * kHalfBytes;
@@ -515,10 +531,6 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         const bool active = t < g.n_main;
         const bool valid_row = active && row_local < g.rpt && r < g.R;
         const int node = valid_row ? (g.r0 + r) / g.G : 0;
-        const bool real = valid_row && node < g.nn;
-        uint32_t visw[4] = {0u, 0u, 0u, 0u};
-        if (real)
-            for (int w = 0; w < p.W; ++w) visw[w] = p.vis[(static_cast<size_t>(g.b) * p.N + node) * p.W + w];
         const uint32_t lane_off = static_cast<uint32_t>(32 * qw) << 16;
         const uint32_t tS = tbase + lane_off + kColS + 64 * t;
         const uint32_t tO = tbase + lane_off + kColO + 128 * t;
@@ -546,6 +558,11 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         } else if (t < n_main_all && lane == 0) {
             mbar_arrive(bar_addr(sh.q_tmem));   // a tile this row group does not use
         }
+        read_tree();   // after the Q copy: the tree is first needed by the masks
+        const bool real = valid_row && node < g.nn;
+        uint32_t visw[4] = {0u, 0u, 0u, 0u};
+        if (real)
+            for (int w = 0; w < p.W; ++w) visw[w] = p.vis[(static_cast<size_t>(g.b) * p.N + node) * p.W + w];
         const float sc = p.scale_log2;            // > 0 on this path
         float m_ref = -INFINITY;                  // reference max, scaled log2 units
         float l_sum = 0.0f;
@@ -712,6 +729,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
     } else if (warp >= 12 && side_all && g.n_side == 0) {
         // a row group without leftover rows in a launch whose last group has
         // them: these warps still release every K/V stage the ring counts on
+        read_tree();   // tile_info below uses n_nodes
         bool ok = true;
         for (int j = 0; ok && j < g.n_tiles; ++j) {
             const int s = j % kStages;
@@ -720,6 +738,7 @@ attn_tc_kernel(const AttnParams p, const __grid_constant__ TcMaps maps) {
         }
     } else if (warp >= 12 && g.n_side > 0) {
         // ---------------- leftover rows on mma.sync ----------------
+        read_tree();
         const int sw = warp - 12;                      // keys 16*sw .. 16*sw+15 of each tile
         const int nrow = lane >> 2;                    // B-fragment row (n index)
         const int crow0 = 2 * (lane & 3);              // C-fragment rows crow0, crow0+1
@@ -1011,9 +1030,20 @@ cudaError_t launch_attn_tc(const AttnParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.max_chunks) * p.Hkv * p.tc_groups * p.B;
     if (ctas > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-    if (whole) attn_tc_kernel<true><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(p, maps);
-    else attn_tc_kernel<false><<<static_cast<unsigned>(ctas), kThreads, kSmemBytes, stream>>>(p, maps);
-    return cudaGetLastError();
+    // a programmatic dependent of the build: the context streams while the
+    // build finishes; the tree is read after griddepcontrol.wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return whole ? cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, p, maps)
+                 : cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, p, maps);
 }
 
 }  // namespace ddt

@@ -170,6 +170,9 @@ ddtree_build_kernel(const float* __restrict__ topk_logp, const int32_t* __restri
                     int32_t* dev_status) {
     __shared__ BuildSmem s;
     extern __shared__ __align__(16) unsigned char dyn[];   // staged top-k: D*K doubles then D*K ints
+    // a programmatic dependent (the attention) may start now: it reads this
+    // kernel's outputs only after waiting for the whole grid
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x;
     double* lp = reinterpret_cast<double*>(dyn);
