@@ -46,7 +46,7 @@ METRIC = "tree-verify steps/s & attn HBM GB/s (% roofline), batch16 ctx8k budget
 # dram__bytes_read.sum + dram__bytes_write.sum from an ncu capture (a metric
 # list, one launch) of `bench.py --steps 5 --warmup 3 --no-cpu-baseline
 # --e2e-steps 3`, on the current kernel (profiles/attn_tc_batched16_ctx8k.md).
-ATTN_TC_TRAFFIC_BYTES = 533580544 + 25411072
+ATTN_TC_TRAFFIC_BYTES = 533692672 + 25800448
 L2_FLUSH_BELOW = 256e6   # a paged KV cache smaller than this is timed with L2 flushed
 WORKLOAD_DESC = ("batched serving: 16 requests, ctx ~U[1024,16384] paged (page 64, shuffled), "
                  "Hq 64 / Hkv 8 / Dh 128 bf16, budget 32 (N=33), top-k 8, depth 8, vocab 32000")
