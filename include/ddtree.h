@@ -343,6 +343,10 @@ int ddtree_accept_sample(const float* logits, int V, const int32_t* token,
  * writes for the same inputs. Device errors: the union of the two calls'.
  * Errors: as the two calls (the same argument checks, applied to both output
  * sets).
+ * The kernel is launched as a programmatic dependent of the work before it
+ * on the stream and reads nothing until that work's grid has completed, so
+ * only its launch overlaps (the split-KV merge of tree_verify_attn lets it
+ * start early).
  */
 int ddtree_accept_greedy_sample(const float* logits, int V, const int32_t* token,
                                 const int32_t* first_child, const int32_t* next_sibling,

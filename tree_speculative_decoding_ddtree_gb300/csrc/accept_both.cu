@@ -17,7 +17,9 @@
 // the second pass over the row is served from the caches. Every pass, every
 // reduction and every decision is the one ddtree_accept_greedy and
 // ddtree_accept_sample make, in the same order, so the outputs are
-// bit-identical to those two calls.
+// bit-identical to those two calls. The launch is a programmatic dependent of
+// the work before it (the split-KV merge signals early); the kernel reads
+// nothing before griddepcontrol.wait.
 #include "walk.cuh"
 
 namespace ddt {
@@ -30,6 +32,9 @@ accept_both_kernel(const float* __restrict__ logits, int V, bool vec4,
                    const int32_t* __restrict__ next_sibling, const int32_t* __restrict__ n_nodes,
                    int N, int D, const float* __restrict__ temperature, const uint64_t* __restrict__ seed,
                    uint64_t offset, WalkOut og, WalkOut os, int32_t* dev_status) {
+    // a programmatic dependent of the work before it: nothing is read before
+    // that work's grid has completed
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     __shared__ unsigned long long scratch_a[32];   // greedy argmax reduction
     __shared__ unsigned long long scratch_u[32];   // bonus reduction
     __shared__ float scratch_m[32];
@@ -361,10 +366,18 @@ cudaError_t launch_accept_both(const float* logits, int V, const int32_t* token,
                                const float* temperature, const uint64_t* seed, uint64_t offset,
                                const WalkOut& og, const WalkOut& os, int32_t* dev_status, cudaStream_t stream) {
     const bool vec4 = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
-    accept_both_kernel<<<B * kCluster, kWalkThreads, 0, stream>>>(logits, V, vec4, token, first_child,
-                                                                  next_sibling, n_nodes, N, D, temperature,
-                                                                  seed, offset, og, os, dev_status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B) * kCluster);
+    cfg.blockDim = dim3(kWalkThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_both_kernel, logits, V, vec4, token, first_child, next_sibling,
+                              n_nodes, N, D, temperature, seed, offset, og, os, dev_status);
 }
 
 }  // namespace ddt

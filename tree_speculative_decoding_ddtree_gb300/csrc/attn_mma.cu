@@ -307,6 +307,7 @@ attn_mma_kernel(AttnParams p) {
 template <int DH>
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(AttnParams p) {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");   // the walk may start; it waits for this grid
     const int b = blockIdx.z, kvh = blockIdx.y;
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -386,6 +387,7 @@ static_assert(32 % kMergeBatch == 0, "a batch of chunks stays within one lane wo
 template <int DH>
 __global__ void __launch_bounds__(256)
 attn_combine_wide_kernel(AttnParams p) {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");   // the walk may start; it waits for this grid
     const int b = blockIdx.z, kvh = blockIdx.y;
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
